@@ -1,0 +1,181 @@
+/*
+ * pa.h -- C ABI of libpa_gb300: batched attention over a paged key/value pool
+ * for a continuous-batching engine, on one NVIDIA GB300 (sm_103a).
+ *
+ * What it computes ("GPU inference engine engineering", section "Batching
+ * without running out of cache"; "Building an LLM runtime from scratch on
+ * NVIDIA H100", section "Bug #1"; "llm-rs: LLM Inference in Rust ...",
+ * section "4. Going down a level: SIMT kernels"):
+ *   - K/V live in a pool of fixed-size pages; each sequence owns a block table
+ *     mapping its logical page j (tokens j*P .. j*P+P-1) to a physical page.
+ *   - A step is a set of rows; each row carries its own query, sequence id and
+ *     position.  pa_append_kv scatters the rows' new keys and values into their
+ *     page slots; pa_attention then computes, for every row r and query head g,
+ *         out[r][g] = softmax_t( scale * q[r][g] . K_s[t] ) . V_s[t],  t = 0..position
+ *     over the row's own sequence s, with kv head g / (Hq / Hkv) (grouped-query
+ *     heads), an FP32 online softmax, and a split-KV path for long contexts whose
+ *     partial (max, sum, acc) triples are merged in a fixed order.
+ *   - Rows listed in a prefill chunk (consecutive rows of one sequence at
+ *     consecutive positions) run on a tensor-core tile path in the same launch.
+ *
+ * Conventions for every entry point:
+ *   - All device memory (pools, q, k/v, out, tables, workspace, status) is
+ *     allocated and owned by the caller.  The library owns only the small host
+ *     pa_pool object.  No call allocates device memory or synchronises.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Host-side argument errors return a status at once, launch nothing, and
+ *     set a thread-local message readable with pa_last_error().  No C++
+ *     exception crosses the ABI.
+ *   - Device-side errors (a sequence id, position or page id out of range, a
+ *     bounded wait that ran out) are recorded in *status_dev (int32 in device
+ *     memory, may be NULL): the first error code wins (compare-and-swap from
+ *     PA_OK).  The caller zeroes it and reads it back when it wants to know.
+ *     Rows hit by such an error get unspecified output (zeros for rows whose
+ *     sequence id or position is invalid); the kernels never trap.
+ *
+ * Layouts (row-major, innermost last):
+ *   k_pool, v_pool   [num_pages][Hkv][P][D]     kv_dtype, 16-byte aligned
+ *   q, out           [n_rows][Hq][D]            q_dtype (out has q's dtype)
+ *   k_new, v_new     [n_rows][Hkv][D]           in_dtype
+ *   seq_ids, positions [n_rows]                 int32
+ *   block_tables     [num_seqs][max_blocks_per_seq] int32, unused entries -1
+ */
+#ifndef PA_GB300_H
+#define PA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* host-side: a bad pointer, size, dtype or alignment */
+    PA_ERR_UNSUPPORTED = 2, /* host-side: a valid but unimplemented shape (e.g. head_dim 96) */
+    PA_ERR_OUT_OF_RANGE = 3, /* device-side: sequence id, position or page id out of range */
+    PA_ERR_TIMEOUT = 4,     /* device-side: a bounded wait on a copy gave up */
+    PA_ERR_CUDA = 5         /* a CUDA runtime call failed (launch, attribute, driver entry point) */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
+
+/* Pool geometry.  page_size in {16, 32, 64}; head_dim in {64, 128};
+ * kv_dtype PA_F32, PA_BF16 or PA_FP8_E4M3.  k_scale / v_scale are the fp8
+ * per-tensor scales ("Engines for the card you have", section "One checkpoint,
+ * many engines": an FP8 key/value cache, calibrated): a stored code c means
+ * value(c) * scale, and appending x stores e4m3_satfinite_rne(x / scale).
+ * They are ignored (taken as 1) for f32 and bf16 pools. */
+typedef struct {
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    pa_dtype kv_dtype;
+    float k_scale;
+    float v_scale;
+} pa_pool_desc;
+
+typedef struct pa_pool pa_pool; /* opaque host object */
+
+/* Rows row_begin .. row_begin + n_rows - 1 of a step form one causal prefill
+ * chunk: they must share one sequence id and have consecutive increasing
+ * positions.  Host memory. */
+typedef struct {
+    int32_t row_begin;
+    int32_t n_rows;
+} pa_chunk;
+
+/* Bytes of ONE of the two pool buffers (K or V) for this geometry: the memory
+ * need, computed without allocating ("GPU inference engine engineering",
+ * "Batching without running out of cache": the engine computes its memory need
+ * without allocating).  Returns 0 for an invalid descriptor. */
+size_t pa_pool_bytes(const pa_pool_desc *desc);
+
+/* Wrap caller-owned device buffers k_pool and v_pool (each pa_pool_bytes(desc)
+ * bytes, 16-byte aligned) in a host object.  Contents are not touched.
+ * Errors: PA_ERR_INVALID_ARG (NULL pointer, misaligned buffer, non-positive
+ * sizes, fp8 scale not finite and > 0), PA_ERR_UNSUPPORTED (page_size or
+ * head_dim outside the supported sets). */
+pa_status pa_pool_create(const pa_pool_desc *desc, void *k_pool, void *v_pool, pa_pool **out);
+
+/* Free the host object (not the device buffers).  NULL is allowed. */
+void pa_pool_destroy(pa_pool *pool);
+
+/* K/V append ("GPU inference engine engineering", "Batching without running
+ * out of cache"): for each row r, kv head h and element d,
+ *     pool[block_tables[s][p / P]][h][p % P][d] = enc(new[r][h][d]),  s = seq_ids[r], p = positions[r]
+ * for K and V.  enc is a copy (f32->f32, bf16->bf16, bf16->f32 widening),
+ * fp32->bf16 round-to-nearest-even, or for fp8 pools e4m3 satfinite
+ * round-to-nearest-even of (x / scale) with one IEEE binary32 division.
+ * in_dtype is PA_F32 or PA_BF16.  One launch on `stream`.
+ * Precondition: no two rows of one call write the same (page, slot); shared
+ * prefix pages are never append targets.  n_rows == 0 is a no-op.
+ * Device-side: a row with s outside [0, num_seqs), p outside
+ * [0, max_blocks_per_seq * P) or a page id outside [0, num_pages) is skipped
+ * and records PA_ERR_OUT_OF_RANGE. */
+pa_status pa_append_kv(const pa_pool *pool, int32_t n_rows, const void *k_new, const void *v_new,
+                       pa_dtype in_dtype, const int32_t *seq_ids, const int32_t *positions,
+                       const int32_t *block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                       int32_t *status_dev, void *stream);
+
+/* Workspace bytes pa_attention needs for this many rows and this block-table
+ * width (the split-KV partial triples and their per-(row, kv head) counters).
+ * 0 when no row can be split.  Computed on the host from sizes only. */
+size_t pa_attention_workspace_bytes(const pa_pool *pool, int32_t n_rows, int32_t num_q_heads,
+                                    int32_t max_blocks_per_seq);
+
+/* Paged attention over a step's rows (see the top of this file).
+ *   q_dtype      PA_F32 or PA_BF16; out has the same dtype, rounded to nearest even
+ *   num_q_heads  a multiple of the pool's num_kv_heads, with Hq / Hkv in 1..8
+ *   chunks       host array of n_chunks prefill chunks (may be NULL when n_chunks == 0);
+ *                at most 16 chunks.  Rows not in a chunk are decode rows.
+ *   softmax_scale <= 0 selects 1 / sqrt(head_dim)
+ *   workspace    device memory of at least pa_attention_workspace_bytes(...), 256-byte
+ *                aligned, ZERO-FILLED BEFORE ITS FIRST USE; every call leaves it
+ *                zero-filled again, so it is reused without clearing.  Calls that share a
+ *                workspace must not overlap on the GPU.  May be NULL when 0 bytes are needed.
+ * Each row attends keys 0..positions[r] of its own sequence (its own token
+ * included, so append the step's rows first).  A row's output bits depend only
+ * on that row's inputs and on the rows of its own chunk, never on the other
+ * rows of the call or the physical placement of its pages.
+ * One launch on `stream` (a second, tiny launch only when a chunk row's
+ * attention is split); no allocation; graph-capturable. */
+pa_status pa_attention(const pa_pool *pool, int32_t n_rows, const void *q, pa_dtype q_dtype,
+                       int32_t num_q_heads, const int32_t *seq_ids, const int32_t *positions,
+                       const int32_t *block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                       const pa_chunk *chunks, int32_t n_chunks, float softmax_scale, void *out,
+                       void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream);
+
+/* Split-KV chunk length in tokens: a row at position p is cut into
+ * ceil((p + 1) / split) pieces merged in ascending order.  A process-wide
+ * constant (default 1024), a multiple of 64, never derived from the batch.
+ * Changing it changes output bits (within tolerance) for rows longer than it.
+ * Returns PA_ERR_INVALID_ARG for a value that is not a positive multiple of 64. */
+pa_status pa_set_split_tokens(int32_t tokens);
+int32_t pa_get_split_tokens(void);
+
+/* Upper bound on the polls of one device-side wait before it gives up with
+ * PA_ERR_TIMEOUT (0 restores the default of about a second).  A debugging
+ * knob: with 1, waits give up almost at once, which exercises the error path
+ * without any real hang. */
+void pa_set_wait_limit(uint32_t polls);
+
+const char *pa_status_string(pa_status status);
+
+/* Detail text of the last host-side error on this thread ("" if none). */
+const char *pa_last_error(void);
+
+/* Number of CUDA kernels this library has launched in this process (all
+ * entry points, all devices): lets a caller count the launches of a region. */
+uint64_t pa_kernel_launches(void);
+
+/* Library version string. */
+const char *pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_GB300_H */

@@ -1,0 +1,284 @@
+// pa_api.cu -- the C ABI declared in include/pa.h: argument validation, launch
+// geometry and dispatch.  No allocation, no device synchronisation.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "../../include/pa.h"
+#include "pa_kernels.h"
+
+struct pa_pool {
+  pa_pool_desc desc;
+  void* k;
+  void* v;
+};
+
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+
+void pa::count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+int32_t g_split_tokens = pa::kDefaultSplitTokens;
+uint32_t g_wait_limit = pa::kDefaultWaitLimit;
+
+pa_status fail(pa_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+pa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t elt_bytes(pa_dtype t) { return t == PA_F32 ? 4 : t == PA_BF16 ? 2 : 1; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Decode pipeline depth: about 64 KiB of stage ring per CTA (three CTAs per SM).
+int decode_stages(const pa_pool_desc& d) {
+  const size_t page_pair = 2 * static_cast<size_t>(d.page_size) * d.head_dim * elt_bytes(d.kv_dtype);
+  int n = static_cast<int>((64 * 1024) / page_pair);
+  if (n < 2) n = 2;
+  if (n > pa::kMaxStages) n = pa::kMaxStages;
+  return n;
+}
+
+int max_splits_for(const pa_pool_desc& d, int32_t max_blocks) {
+  const long long cap = static_cast<long long>(max_blocks) * d.page_size;
+  return static_cast<int>((cap + g_split_tokens - 1) / g_split_tokens);
+}
+
+// Workspace layout: [counters: n_rows*Hkv int32, padded to 256 B][ml: n_rows*Hq*S*2 f32][o: n_rows*Hq*S*D f32]
+struct WsLayout {
+  size_t count_off, ml_off, o_off, total;
+};
+
+WsLayout ws_layout(const pa_pool_desc& d, int32_t n_rows, int32_t hq, int max_splits) {
+  WsLayout w{0, 0, 0, 0};
+  if (max_splits <= 1 || n_rows <= 0) return w;
+  auto pad = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t slots = static_cast<size_t>(n_rows) * hq * max_splits;
+  w.count_off = 0;
+  w.ml_off = pad(static_cast<size_t>(n_rows) * d.num_kv_heads * sizeof(int32_t));
+  w.o_off = w.ml_off + pad(slots * 2 * sizeof(float));
+  w.total = w.o_off + pad(slots * d.head_dim * sizeof(float));
+  return w;
+}
+
+pa_status check_desc(const pa_pool_desc* d) {
+  if (d == nullptr) return fail(PA_ERR_INVALID_ARG, "pool descriptor is NULL");
+  if (d->num_pages <= 0 || d->num_kv_heads <= 0 || d->page_size <= 0 || d->head_dim <= 0)
+    return fail(PA_ERR_INVALID_ARG, "pool sizes must be positive (pages %d, kv heads %d, page %d, head_dim %d)",
+                d->num_pages, d->num_kv_heads, d->page_size, d->head_dim);
+  if (d->kv_dtype != PA_F32 && d->kv_dtype != PA_BF16 && d->kv_dtype != PA_FP8_E4M3)
+    return fail(PA_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(d->kv_dtype));
+  if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
+    return fail(PA_ERR_UNSUPPORTED, "page_size %d not in {16, 32, 64}", d->page_size);
+  if (d->head_dim != 64 && d->head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}", d->head_dim);
+  if (d->kv_dtype == PA_FP8_E4M3 &&
+      !(std::isfinite(d->k_scale) && d->k_scale > 0.f && std::isfinite(d->v_scale) && d->v_scale > 0.f))
+    return fail(PA_ERR_INVALID_ARG, "fp8 scales must be finite and positive (k %g, v %g)", d->k_scale, d->v_scale);
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_pool_bytes(const pa_pool_desc* desc) {
+  if (check_desc(desc) != PA_OK) return 0;
+  return static_cast<size_t>(desc->num_pages) * desc->num_kv_heads * desc->page_size * desc->head_dim *
+         elt_bytes(desc->kv_dtype);
+}
+
+pa_status pa_pool_create(const pa_pool_desc* desc, void* k_pool, void* v_pool, pa_pool** out) {
+  if (out == nullptr) return fail(PA_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (k_pool == nullptr || v_pool == nullptr) return fail(PA_ERR_INVALID_ARG, "pool buffers must not be NULL");
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16)) return fail(PA_ERR_INVALID_ARG, "pool buffers must be 16-byte aligned");
+  pa_pool* p = new (std::nothrow) pa_pool;
+  if (p == nullptr) return fail(PA_ERR_INVALID_ARG, "out of host memory");
+  p->desc = *desc;
+  if (p->desc.kv_dtype != PA_FP8_E4M3) p->desc.k_scale = p->desc.v_scale = 1.0f;
+  p->k = k_pool;
+  p->v = v_pool;
+  *out = p;
+  return PA_OK;
+}
+
+void pa_pool_destroy(pa_pool* pool) { delete pool; }
+
+pa_status pa_append_kv(const pa_pool* pool, int32_t n_rows, const void* k_new, const void* v_new, pa_dtype in_dtype,
+                       const int32_t* seq_ids, const int32_t* positions, const int32_t* block_tables,
+                       int32_t num_seqs, int32_t max_blocks_per_seq, int32_t* status_dev, void* stream) {
+  if (pool == nullptr) return fail(PA_ERR_INVALID_ARG, "pool is NULL");
+  if (n_rows < 0) return fail(PA_ERR_INVALID_ARG, "n_rows %d < 0", n_rows);
+  if (n_rows == 0) return PA_OK;
+  if (in_dtype != PA_F32 && in_dtype != PA_BF16)
+    return fail(PA_ERR_INVALID_ARG, "append input dtype must be f32 or bf16");
+  if (!k_new || !v_new || !seq_ids || !positions || !block_tables)
+    return fail(PA_ERR_INVALID_ARG, "append: a device pointer is NULL");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16)) return fail(PA_ERR_INVALID_ARG, "k_new / v_new must be 16-byte aligned");
+  if (num_seqs <= 0 || max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_seqs and max_blocks_per_seq must be positive");
+  pa::AppendParams p{};
+  p.k_pool = pool->k;
+  p.v_pool = pool->v;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.seq_ids = seq_ids;
+  p.positions = positions;
+  p.block_tables = block_tables;
+  p.n_rows = n_rows;
+  p.num_seqs = num_seqs;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_pages = pool->desc.num_pages;
+  p.P = pool->desc.page_size;
+  p.Hkv = pool->desc.num_kv_heads;
+  p.D = pool->desc.head_dim;
+  p.in_dtype = in_dtype == PA_F32 ? pa::KV_F32 : pa::KV_BF16;
+  p.kv_dtype = static_cast<int32_t>(pool->desc.kv_dtype);
+  p.k_scale = pool->desc.k_scale;
+  p.v_scale = pool->desc.v_scale;
+  p.status = status_dev;
+  cudaError_t e = pa::launch_append(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return PA_OK;
+}
+
+size_t pa_attention_workspace_bytes(const pa_pool* pool, int32_t n_rows, int32_t num_q_heads,
+                                    int32_t max_blocks_per_seq) {
+  if (pool == nullptr || n_rows <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0) return 0;
+  return ws_layout(pool->desc, n_rows, num_q_heads, max_splits_for(pool->desc, max_blocks_per_seq)).total;
+}
+
+pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dtype q_dtype, int32_t num_q_heads,
+                       const int32_t* seq_ids, const int32_t* positions, const int32_t* block_tables,
+                       int32_t num_seqs, int32_t max_blocks_per_seq, const pa_chunk* chunks, int32_t n_chunks,
+                       float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
+                       int32_t* status_dev, void* stream) {
+  if (pool == nullptr) return fail(PA_ERR_INVALID_ARG, "pool is NULL");
+  const pa_pool_desc& d = pool->desc;
+  if (n_rows < 0) return fail(PA_ERR_INVALID_ARG, "n_rows %d < 0", n_rows);
+  if (q_dtype != PA_F32 && q_dtype != PA_BF16) return fail(PA_ERR_INVALID_ARG, "q dtype must be f32 or bf16");
+  if (num_q_heads <= 0 || num_q_heads % d.num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d", num_q_heads,
+                d.num_kv_heads);
+  const int G = num_q_heads / d.num_kv_heads;
+  if (G > 8) return fail(PA_ERR_UNSUPPORTED, "query heads per kv head %d > 8", G);
+  if (num_seqs <= 0 || max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_seqs and max_blocks_per_seq must be positive");
+  if (n_chunks < 0 || n_chunks > pa::kMaxChunks)
+    return fail(PA_ERR_INVALID_ARG, "n_chunks %d outside [0, %d]", n_chunks, pa::kMaxChunks);
+  if (n_chunks > 0 && chunks == nullptr) return fail(PA_ERR_INVALID_ARG, "chunks is NULL");
+  for (int c = 0; c < n_chunks; ++c) {
+    if (chunks[c].n_rows <= 0 || chunks[c].row_begin < 0 ||
+        static_cast<long long>(chunks[c].row_begin) + chunks[c].n_rows > n_rows)
+      return fail(PA_ERR_INVALID_ARG, "chunk %d rows [%d, +%d) outside [0, %d)", c, chunks[c].row_begin,
+                  chunks[c].n_rows, n_rows);
+    for (int c2 = 0; c2 < c; ++c2)
+      if (chunks[c].row_begin < chunks[c2].row_begin + chunks[c2].n_rows &&
+          chunks[c2].row_begin < chunks[c].row_begin + chunks[c].n_rows)
+        return fail(PA_ERR_INVALID_ARG, "chunks %d and %d overlap", c2, c);
+  }
+  if (n_rows == 0) return PA_OK;
+  if (!q || !seq_ids || !positions || !block_tables || !out)
+    return fail(PA_ERR_INVALID_ARG, "attention: a device pointer is NULL");
+  const int max_splits = max_splits_for(d, max_blocks_per_seq);
+  const WsLayout ws = ws_layout(d, n_rows, num_q_heads, max_splits);
+  if (ws.total > 0) {
+    if (workspace == nullptr || workspace_bytes < ws.total)
+      return fail(PA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", ws.total,
+                  workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);
+    if (!aligned(workspace, 256)) return fail(PA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+  const double sm = softmax_scale > 0.f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt(static_cast<double>(d.head_dim));
+  const double k_scale = d.kv_dtype == PA_FP8_E4M3 ? static_cast<double>(d.k_scale) : 1.0;
+
+  pa::AttnParams p{};
+  p.k_pool = pool->k;
+  p.v_pool = pool->v;
+  p.q = q;
+  p.out = out;
+  p.seq_ids = seq_ids;
+  p.positions = positions;
+  p.block_tables = block_tables;
+  p.n_rows = n_rows;
+  p.num_seqs = num_seqs;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_pages = d.num_pages;
+  p.P = d.page_size;
+  p.Hq = num_q_heads;
+  p.Hkv = d.num_kv_heads;
+  p.D = d.head_dim;
+  p.q_is_bf16 = q_dtype == PA_BF16;
+  p.split_tokens = g_split_tokens;
+  p.max_splits = max_splits;
+  p.qk_scale_log2 = static_cast<float>(sm * k_scale * 1.4426950408889634073599246810018921);  // log2(e)
+  p.v_scale = d.kv_dtype == PA_FP8_E4M3 ? d.v_scale : 1.0f;
+  if (ws.total > 0) {
+    unsigned char* base = static_cast<unsigned char*>(workspace);
+    p.ws_count = reinterpret_cast<int32_t*>(base + ws.count_off);
+    p.ws_ml = reinterpret_cast<float*>(base + ws.ml_off);
+    p.ws_o = reinterpret_cast<float*>(base + ws.o_off);
+  }
+  p.status = status_dev;
+  p.wait_limit = g_wait_limit;
+  p.n_stages = decode_stages(d);
+  p.n_prefill_ctas = 0;
+  p.n_chunks = 0;  // chunk rows run on the decode path until the tile path takes them
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (d.kv_dtype) {
+    case PA_F32: e = pa::launch_decode_f32(p, s); break;
+    case PA_BF16: e = pa::launch_decode_bf16(p, s); break;
+    default: e = pa::launch_decode_e4m3(p, s); break;
+  }
+  if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "no decode kernel for head_dim %d, group %d", d.head_dim, G);
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return PA_OK;
+}
+
+pa_status pa_set_split_tokens(int32_t tokens) {
+  if (tokens <= 0 || tokens % 64 != 0) return fail(PA_ERR_INVALID_ARG, "split tokens %d is not a positive multiple of 64", tokens);
+  g_split_tokens = tokens;
+  return PA_OK;
+}
+
+int32_t pa_get_split_tokens(void) { return g_split_tokens; }
+
+void pa_set_wait_limit(uint32_t polls) { g_wait_limit = polls == 0 ? pa::kDefaultWaitLimit : polls; }
+
+const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_OUT_OF_RANGE: return "PA_ERR_OUT_OF_RANGE";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+const char* pa_last_error(void) { return g_last_error; }
+
+uint64_t pa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* pa_version(void) { return "paged_kv_continuous_pa_gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

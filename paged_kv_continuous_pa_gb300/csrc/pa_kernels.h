@@ -1,0 +1,81 @@
+// pa_kernels.h -- launch parameters shared by the host API (pa_api.cu) and the
+// kernels.  Internal: not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kMaxChunks = 16;          // prefill chunks per pa_attention call
+constexpr int kDefaultSplitTokens = 1024;
+constexpr uint32_t kDefaultWaitLimit = 1u << 22;  // polls of one bounded wait (about a second)
+constexpr uint32_t kDrainWaitLimit = 1u << 22;    // polls spent draining copies on an error path
+constexpr int kMaxStages = 16;          // decode pipeline depth upper bound
+constexpr int kDecodeWarps = 4;         // consumer warps of a decode CTA (+1 producer warp)
+
+enum KvType { KV_F32 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
+
+// Device status codes (same values as pa_status in include/pa.h).
+enum { ST_OK = 0, ST_OUT_OF_RANGE = 3, ST_TIMEOUT = 4 };
+
+struct AppendParams {
+  void* k_pool;
+  void* v_pool;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* seq_ids;
+  const int32_t* positions;
+  const int32_t* block_tables;
+  int32_t n_rows, num_seqs, max_blocks, num_pages;
+  int32_t P, Hkv, D;
+  int32_t in_dtype;  // KV_F32 or KV_BF16
+  int32_t kv_dtype;  // KvType
+  float k_scale, v_scale;
+  int32_t* status;
+};
+
+struct AttnParams {
+  const void* k_pool;
+  const void* v_pool;
+  const void* q;
+  void* out;
+  const int32_t* seq_ids;
+  const int32_t* positions;
+  const int32_t* block_tables;
+  int32_t n_rows, num_seqs, max_blocks, num_pages;
+  int32_t P, Hq, Hkv, D;
+  int32_t q_is_bf16;
+  int32_t split_tokens;  // split-KV chunk length (multiple of P)
+  int32_t max_splits;    // ceil(max_blocks * P / split_tokens)
+  float qk_scale_log2;   // softmax scale * log2(e) * k_scale (scores live in the log2 domain)
+  float v_scale;         // fp8 value scale, 1 otherwise
+  float* ws_o;           // [n_rows][Hq][max_splits][D] partial accumulators (split rows only)
+  float* ws_ml;          // [n_rows][Hq][max_splits][2] partial (max, sum)
+  int32_t* ws_count;     // [n_rows][Hkv] finished-split counters, zero between calls
+  int32_t* status;
+  uint32_t wait_limit;
+  int32_t n_stages;      // decode pipeline depth
+  int32_t n_prefill_ctas;  // CTAs [0, n_prefill_ctas) run prefill tiles, the rest decode units
+  int32_t n_chunks;
+  int32_t chunk_begin[kMaxChunks];
+  int32_t chunk_end[kMaxChunks];
+};
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+
+// Process-wide count of kernel launches made by the library (pa_kernel_launches).
+void count_launch();
+
+// Decode-unit kernels, one translation unit per K/V dtype.  Return
+// cudaErrorNotSupported for a (G, D) pair without an instantiation.
+cudaError_t launch_decode_f32(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_decode_e4m3(const AttnParams& p, cudaStream_t stream);
+
+// Dynamic shared memory a decode CTA needs for this geometry (0 = no instantiation).
+size_t decode_smem_bytes_f32(int P, int D, int G, int n_stages);
+size_t decode_smem_bytes_bf16(int P, int D, int G, int n_stages);
+size_t decode_smem_bytes_e4m3(int P, int D, int G, int n_stages);
+
+}  // namespace pa

@@ -1,0 +1,114 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every function include/pa.h declares, and its host-side argument checks
+return the documented status codes without launching anything."""
+import ctypes
+
+import pytest
+
+import paged_kv_continuous_pa_gb300 as pa
+from paged_kv_continuous_pa_gb300 import build as pa_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pa_build.build()
+    return pa.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = pa.header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/pa.h but not exported"
+
+
+def test_no_oracle_symbols_in_library(lib):
+    for n in ("oracle_attention", "oracle_append", "oracle_e4m3_from_f32"):
+        with pytest.raises(AttributeError):
+            getattr(lib, n)
+
+
+def _desc(**kw):
+    d = dict(num_pages=16, page_size=32, num_kv_heads=2, head_dim=64, kv_dtype=pa.PA_BF16, k_scale=1.0, v_scale=1.0)
+    d.update(kw)
+    return pa.PoolDesc(**d)
+
+
+def test_pool_bytes(lib):
+    assert lib.pa_pool_bytes(ctypes.byref(_desc())) == 16 * 2 * 32 * 64 * 2
+    assert lib.pa_pool_bytes(ctypes.byref(_desc(kv_dtype=pa.PA_FP8_E4M3, k_scale=0.1, v_scale=0.1))) == 16 * 2 * 32 * 64
+    assert lib.pa_pool_bytes(ctypes.byref(_desc(kv_dtype=pa.PA_F32))) == 16 * 2 * 32 * 64 * 4
+    assert lib.pa_pool_bytes(ctypes.byref(_desc(head_dim=96))) == 0
+    assert lib.pa_pool_bytes(None) == 0
+
+
+def _create(lib, desc, k=0x10000, v=0x20000):
+    h = ctypes.c_void_p()
+    st = lib.pa_pool_create(ctypes.byref(desc), ctypes.c_void_p(k), ctypes.c_void_p(v), ctypes.byref(h))
+    return st, h
+
+
+def test_pool_create_validation(lib):
+    st, h = _create(lib, _desc())
+    assert st == pa.PA_OK and h.value
+    lib.pa_pool_destroy(h)
+    assert _create(lib, _desc(head_dim=96))[0] == pa.PA_ERR_UNSUPPORTED
+    assert _create(lib, _desc(page_size=8))[0] == pa.PA_ERR_UNSUPPORTED
+    assert _create(lib, _desc(num_pages=0))[0] == pa.PA_ERR_INVALID_ARG
+    assert _create(lib, _desc(kv_dtype=7))[0] == pa.PA_ERR_INVALID_ARG
+    assert _create(lib, _desc(kv_dtype=pa.PA_FP8_E4M3, k_scale=0.0))[0] == pa.PA_ERR_INVALID_ARG
+    assert _create(lib, _desc(kv_dtype=pa.PA_FP8_E4M3, v_scale=float("inf")))[0] == pa.PA_ERR_INVALID_ARG
+    assert _create(lib, _desc(), k=0x10008)[0] == pa.PA_ERR_INVALID_ARG  # not 16-byte aligned
+    assert _create(lib, _desc(), k=0)[0] == pa.PA_ERR_INVALID_ARG
+    assert "aligned" in pa.last_error() or "NULL" in pa.last_error()
+
+
+def test_host_side_errors_launch_nothing(lib):
+    st, h = _create(lib, _desc())
+    assert st == pa.PA_OK
+    try:
+        vp = ctypes.c_void_p
+        dev = vp(0x100000)
+        # bad input dtype
+        assert lib.pa_append_kv(h, 4, dev, dev, pa.PA_FP8_E4M3, dev, dev, dev, 4, 4, None, None) == pa.PA_ERR_INVALID_ARG
+        # zero rows is a no-op
+        assert lib.pa_append_kv(h, 0, None, None, pa.PA_BF16, None, None, None, 4, 4, None, None) == pa.PA_OK
+        # misaligned k_new
+        assert lib.pa_append_kv(h, 4, vp(0x100004), dev, pa.PA_BF16, dev, dev, dev, 4, 4, None, None) == pa.PA_ERR_INVALID_ARG
+        att = lambda **kw: lib.pa_attention(h, kw.get("n", 4), dev, kw.get("qd", pa.PA_BF16), kw.get("hq", 8), dev,
+                                            dev, dev, 4, kw.get("mb", 4), kw.get("chunks"), kw.get("nc", 0), 0.0,
+                                            kw.get("out", dev), kw.get("ws"), kw.get("wsb", 0), None, None)
+        assert att(hq=5) == pa.PA_ERR_INVALID_ARG
+        assert att(hq=18) == pa.PA_ERR_UNSUPPORTED         # group of 9
+        assert att(qd=pa.PA_FP8_E4M3) == pa.PA_ERR_INVALID_ARG
+        assert att(out=None) == pa.PA_ERR_INVALID_ARG
+        assert att(n=0, out=None) == pa.PA_OK
+        two = (pa.Chunk * 2)(pa.Chunk(0, 3), pa.Chunk(2, 2))
+        assert att(chunks=two, nc=2) == pa.PA_ERR_INVALID_ARG   # overlapping chunks
+        assert att(chunks=None, nc=1) == pa.PA_ERR_INVALID_ARG
+        assert att(nc=17) == pa.PA_ERR_INVALID_ARG
+        # long tables need a workspace for split partials
+        need = lib.pa_attention_workspace_bytes(h, 4, 8, 200)
+        assert need > 0 and need % 256 == 0
+        assert att(mb=200) == pa.PA_ERR_INVALID_ARG
+        assert att(mb=200, ws=vp(0x200000), wsb=need - 1) == pa.PA_ERR_INVALID_ARG
+        assert att(mb=200, ws=vp(0x200010), wsb=need) == pa.PA_ERR_INVALID_ARG  # not 256-aligned
+        assert lib.pa_attention_workspace_bytes(h, 4, 8, 4) == 0  # 128 tokens: never split
+    finally:
+        lib.pa_pool_destroy(h)
+
+
+def test_split_tokens_setting(lib):
+    old = lib.pa_get_split_tokens()
+    try:
+        assert lib.pa_set_split_tokens(100) == pa.PA_ERR_INVALID_ARG
+        assert lib.pa_set_split_tokens(0) == pa.PA_ERR_INVALID_ARG
+        assert lib.pa_set_split_tokens(512) == pa.PA_OK and lib.pa_get_split_tokens() == 512
+    finally:
+        lib.pa_set_split_tokens(old)
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED", "PA_ERR_OUT_OF_RANGE",
+                                 "PA_ERR_TIMEOUT", "PA_ERR_CUDA"]):
+        assert pa.status_string(code) == name
