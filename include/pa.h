@@ -148,6 +148,29 @@ pa_status pa_attention(const pa_pool *pool, int32_t n_rows, const void *q, pa_dt
                        const pa_chunk *chunks, int32_t n_chunks, float softmax_scale, void *out,
                        void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream);
 
+/* pa_attention without a workspace argument, for callers that cannot allocate
+ * device memory: code handed only its input and output buffers by a host
+ * runtime that owns and budgets all device memory (a plugin interface), or a
+ * serving loop that forbids cudaMalloc after start-up because an allocation on
+ * the hot path can synchronise the device or fail under memory pressure.  The
+ * pages have no counterpart to this entry point; it exists for such callers.
+ * The split-KV partials go to a scratch array of 32 MiB compiled into the
+ * library's device image: every GPU that loads the library holds it until the
+ * process exits, and this call allocates nothing (no cudaMalloc, no cudaFree,
+ * no allocating library routine).  Arguments and results are those of
+ * pa_attention.  A call whose pa_attention_workspace_bytes(...) exceeds 32 MiB
+ * is rejected with PA_ERR_UNSUPPORTED and a message in pa_last_error().
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call shares the one array and finds the previous call's contents in it;
+ * each call clears the part it uses on `stream` first.  Calls that can run at
+ * the same time on the GPU (unordered streams) race on the array. */
+pa_status pa_attention_noalloc(const pa_pool *pool, int32_t n_rows, const void *q, pa_dtype q_dtype,
+                               int32_t num_q_heads, const int32_t *seq_ids, const int32_t *positions,
+                               const int32_t *block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                               const pa_chunk *chunks, int32_t n_chunks, float softmax_scale, void *out,
+                               int32_t *status_dev, void *stream);
+
 /* Split-KV chunk length in tokens: a row at position p is cut into
  * ceil((p + 1) / split) pieces merged in ascending order.  A process-wide
  * constant (default 1024), a multiple of 64, never derived from the batch.

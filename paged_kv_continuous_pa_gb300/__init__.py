@@ -71,6 +71,9 @@ def load(path: str = LIB_PATH):
         L.pa_attention.argtypes = [vp, i32, vp, i32, i32, vp, vp, vp, i32, i32, ctypes.POINTER(Chunk), i32, f32, vp,
                                    vp, sz, vp, vp]
         L.pa_attention.restype = st
+        L.pa_attention_noalloc.argtypes = [vp, i32, vp, i32, i32, vp, vp, vp, i32, i32, ctypes.POINTER(Chunk), i32,
+                                           f32, vp, vp, vp]
+        L.pa_attention_noalloc.restype = st
         L.pa_set_split_tokens.argtypes = [i32]
         L.pa_set_split_tokens.restype = st
         L.pa_get_split_tokens.argtypes = []
@@ -197,6 +200,22 @@ def attention(pool: Pool, q, seq_ids, positions, block_tables, out,
     _check(load().pa_attention(pool.handle, n, _ptr(q), _dtype_code(q), num_q_heads, _ptr(seq_ids), _ptr(positions),
                                _ptr(block_tables), num_seqs, max_blocks, arr if chunks else None, len(chunks),
                                float(softmax_scale), _ptr(out), ws_ptr, ws_len, _ptr(status), _stream(stream)))
+
+
+def attention_noalloc(pool: Pool, q, seq_ids, positions, block_tables, out,
+                      chunks: Sequence[Tuple[int, int]] = (), softmax_scale: float = 0.0, status=None, stream=None):
+    """attention() for callers that cannot allocate: split-KV scratch comes from
+    a fixed 32 MiB array inside the library instead of a workspace tensor."""
+    n = int(seq_ids.shape[0])
+    num_q_heads = int(q.shape[1])
+    num_seqs, max_blocks = (int(x) for x in block_tables.shape)
+    if out.dtype != q.dtype or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must match q's shape and dtype")
+    arr = (Chunk * max(1, len(chunks)))(*[Chunk(int(b), int(c)) for b, c in chunks])
+    _check(load().pa_attention_noalloc(pool.handle, n, _ptr(q), _dtype_code(q), num_q_heads, _ptr(seq_ids),
+                                       _ptr(positions), _ptr(block_tables), num_seqs, max_blocks,
+                                       arr if chunks else None, len(chunks), float(softmax_scale), _ptr(out),
+                                       _ptr(status), _stream(stream)))
 
 
 def set_split_tokens(tokens: int):

@@ -94,6 +94,13 @@ pa_status check_desc(const pa_pool_desc* d) {
 
 }  // namespace
 
+void pa::set_last_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+}
+
 extern "C" {
 
 size_t pa_pool_bytes(const pa_pool_desc* desc) {

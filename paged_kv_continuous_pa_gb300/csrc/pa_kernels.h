@@ -67,6 +67,9 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 // Process-wide count of kernel launches made by the library (pa_kernel_launches).
 void count_launch();
 
+// Set the calling thread's pa_last_error() text.
+void set_last_error(const char* fmt, ...);
+
 // Decode-unit kernels, one translation unit per K/V dtype.  Return
 // cudaErrorNotSupported for a (G, D) pair without an instantiation.
 cudaError_t launch_decode_f32(const AttnParams& p, cudaStream_t stream);
