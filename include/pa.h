@@ -173,7 +173,7 @@ pa_status pa_attention_noalloc(const pa_pool *pool, int32_t n_rows, const void *
 
 /* Split-KV chunk length in tokens: a row at position p is cut into
  * ceil((p + 1) / split) pieces merged in ascending order.  A process-wide
- * constant (default 1024), a multiple of 64, never derived from the batch.
+ * constant (default 4096), a multiple of 64 up to 4096, never derived from the batch.
  * Changing it changes output bits (within tolerance) for rows longer than it.
  * Returns PA_ERR_INVALID_ARG for a value that is not a positive multiple of 64. */
 pa_status pa_set_split_tokens(int32_t tokens);

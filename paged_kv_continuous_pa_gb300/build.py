@@ -44,8 +44,14 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(OBJ_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), variant: str = "") -> str:
+    """Compile and link; returns the library path.  A non-empty `variant` builds
+    a separately named library (objects under _build/<variant>/) with
+    `extra_flags`, e.g. a tuning constant overridden with -D, leaving the
+    default library untouched."""
+    obj_dir = os.path.join(OBJ_DIR, variant) if variant else OBJ_DIR
+    lib_path = os.path.join(LIB_DIR, f"libpa_gb300_{variant}.so") if variant else LIB_PATH
+    os.makedirs(obj_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     heads = _headers()
@@ -53,7 +59,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     jobs = []
     objs = []
     for s in srcs:
-        o = os.path.join(OBJ_DIR, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(obj_dir, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + heads):
             jobs.append((s, o))
@@ -72,14 +78,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if jobs:
         with cf.ThreadPoolExecutor(max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
             list(ex.map(compile_one, jobs))
-    if force or jobs or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs + ["-Xcompiler", "-fPIC"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":  # pragma: no cover

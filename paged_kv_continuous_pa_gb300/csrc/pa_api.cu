@@ -44,15 +44,6 @@ size_t elt_bytes(pa_dtype t) { return t == PA_F32 ? 4 : t == PA_BF16 ? 2 : 1; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Decode pipeline depth: about 64 KiB of stage ring per CTA (three CTAs per SM).
-int decode_stages(const pa_pool_desc& d) {
-  const size_t page_pair = 2 * static_cast<size_t>(d.page_size) * d.head_dim * elt_bytes(d.kv_dtype);
-  int n = static_cast<int>((64 * 1024) / page_pair);
-  if (n < 2) n = 2;
-  if (n > pa::kMaxStages) n = pa::kMaxStages;
-  return n;
-}
-
 int max_splits_for(const pa_pool_desc& d, int32_t max_blocks) {
   const long long cap = static_cast<long long>(max_blocks) * d.page_size;
   return static_cast<int>((cap + g_split_tokens - 1) / g_split_tokens);
@@ -244,7 +235,6 @@ pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dt
   }
   p.status = status_dev;
   p.wait_limit = g_wait_limit;
-  p.n_stages = decode_stages(d);
   p.n_prefill_ctas = 0;
   p.n_chunks = 0;  // chunk rows run on the decode path until the tile path takes them
 
@@ -261,7 +251,8 @@ pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dt
 }
 
 pa_status pa_set_split_tokens(int32_t tokens) {
-  if (tokens <= 0 || tokens % 64 != 0) return fail(PA_ERR_INVALID_ARG, "split tokens %d is not a positive multiple of 64", tokens);
+  if (tokens <= 0 || tokens % 64 != 0 || tokens > pa::kMaxSplitTokens)
+    return fail(PA_ERR_INVALID_ARG, "split tokens %d is not a multiple of 64 in [64, %d]", tokens, pa::kMaxSplitTokens);
   g_split_tokens = tokens;
   return PA_OK;
 }

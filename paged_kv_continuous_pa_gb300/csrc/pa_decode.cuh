@@ -9,23 +9,24 @@
 // decode attention split into chunks of positions, each with its own online
 // softmax, followed by a cheap merge).
 //
-// CTA layout: warps 0..3 consume, warp 4 produces.
-//   producer  one lane issues one 1-D bulk copy per page for K and one for V
-//             (a page of one kv head is contiguous: P*D*elt bytes) into a ring
-//             of shared-memory stages; completion is counted in bytes on the
-//             stage's `full` mbarrier.  The last page of the row copies only its
-//             valid slots.  Page ids are read 32 at a time, one per lane, and
-//             range-checked before any copy is issued.
-//   consumers wait on `full`, compute, then arrive on `empty` (one arrival per
-//             warp).  There is no CTA-wide barrier inside the role branches; the
-//             only __syncthreads are outside them (the bug the H100 page
-//             describes cannot occur).
-// Work split inside a page: the page's tokens are cut into steps of TPS
-// tokens; step k of the unit's page n goes to warp (n * steps_per_page + k) % 4.
-// Within a step, LPT lanes share one token: each lane dots its D / LPT
-// elements of K with the matching slice of the G query vectors held in
-// registers, and a fixed xor-butterfly over the LPT lanes completes the dot
-// product.  For P.V each lane owns D / 32 consecutive output elements.
+// CTA layout: 4 warps, all of them consumers.  The unit's keys are cut into
+// 32-token stages; a stage holds those tokens' K and V rows (for one kv head a
+// page is contiguous, so a stage is one or two 1-D bulk copies per operand:
+// half a 64-token page, a 32-token page, or two 16-token pages), and only the
+// valid slots of the last page are copied.  Stages live in a ring of
+// shared-memory slots whose `full` mbarrier counts the copied bytes.  Thread 0
+// fills the ring at the start; afterwards the LAST warp to finish with a slot
+// (a shared-memory counter) issues the copies of the stage that goes there
+// next, so no warp ever waits for a slot to drain and no producer warp takes
+// registers.  Page ids are read once per unit and range-checked before any
+// copy.  No CTA-wide barrier sits inside a warp-dependent branch (the bug the
+// H100 page describes cannot occur).
+// Work split inside a stage: warp w owns tokens 8w .. 8w+7.  For Q.K, LPT
+// lanes share one token and each dots its D / LPT elements with the matching
+// slice of the G query vectors held in registers; a fixed xor-butterfly over
+// the LPT lanes completes the dot product.  One online-softmax update covers
+// the warp's 8 tokens.  For P.V, PLT lanes share one token and each owns PE
+// consecutive output elements.
 //
 // Determinism: every sum runs in an order fixed by (position, head, element)
 // alone -- FMA chains in a fixed order, fixed shuffle trees, a fixed warp order
@@ -55,33 +56,57 @@ struct KvElt<KV_E4M3> {
 };
 
 // Compile-time geometry of one decode instantiation.
+//   QK layout: LPT lanes share one token; each holds D / LPT elements of the G
+//   query vectors in registers.  A warp scores TPS tokens per sub-step and U
+//   sub-steps cover its 8 tokens of a 32-token stage.
+//   PV layout: PLT lanes share one token; each owns PE consecutive output
+//   elements, so one 4..16-byte shared-memory load feeds G * PE FMAs.
 template <int D, int G, int KVT>
 struct DecodeGeom {
   static constexpr int ELT = KvElt<KVT>::bytes;
   static constexpr int RB = D * ELT;                     // bytes of one K or V row
+  static constexpr int NW = kDecodeWarps;
+  static constexpr int THREADS = NW * 32;
+  static constexpr int ST = kStageTokens;                // tokens per stage
+  static constexpr int WT = ST / NW;                     // tokens per warp per stage
   static constexpr int LPT_MIN = (G * D + 63) / 64;      // keep the query slice at <= 64 registers
-  static constexpr int LPT = LPT_MIN <= 4 ? 4 : (LPT_MIN <= 8 ? 8 : 16);  // lanes per token
-  static constexpr int TPS = 32 / LPT;                   // tokens per warp step
+  static constexpr int LPT = LPT_MIN <= 4 ? 4 : (LPT_MIN <= 8 ? 8 : 16);
+  static constexpr int TPS = 32 / LPT;
+  static constexpr int U = WT / TPS;
   static constexpr int EPL = D / LPT;                    // QK elements per lane
-  static constexpr int LB = EPL * ELT;                   // QK bytes per lane
+  static constexpr int LB = EPL * ELT;
   static constexpr int VEC = LB < 16 ? LB : 16;          // one shared-memory load
   static constexpr int NV = LB / VEC;                    // loads per lane per token
-  static constexpr int EPV = VEC / ELT;                  // elements per load
-  static constexpr int DPL = D / 32;                     // P.V output elements per lane
-  static constexpr int VB = DPL * ELT;                   // P.V bytes per lane
-  static constexpr int NW = kDecodeWarps;
-  static constexpr int THREADS = (NW + 1) * 32;
-  static_assert(D % LPT == 0 && D % 32 == 0, "head_dim");
-  static_assert(LB % VEC == 0, "vector split");
+  static constexpr int EPV = VEC / ELT;
+  static constexpr int PE_CAP = (32 / G) >= 16 ? 16 : (32 / G) >= 8 ? 8 : (32 / G) >= 4 ? 4 : 2;
+  static constexpr int PE_WANT = (D / 32) > PE_CAP ? (D / 32) : PE_CAP;
+  static constexpr int PE = (16 / ELT) < PE_WANT ? (16 / ELT) : PE_WANT;  // P.V elements per lane
+  static constexpr int PLT = D / PE;                     // P.V lanes per token
+  static constexpr int TPV = 32 / PLT;                   // P.V tokens per iteration
+  static constexpr int NPV = WT / TPV;                   // P.V iterations per stage
+  static constexpr int VB = PE * ELT;                    // P.V bytes per lane
+  // Occupancy: four CTAs per SM (128 registers a thread) unless the register
+  // estimate says that would spill, then three (168 registers).  The stage ring
+  // takes what is left of the SM's shared memory at that occupancy.
+  static constexpr int REG_EST = G * EPL + G * PE + U * G + 40;
+  static constexpr int MIN_CTAS = REG_EST > 128 ? 3 : kDecodeMinCtas;
+  static constexpr int RING_BYTES = MIN_CTAS >= 4 ? kDecodeRingBytes : kDecodeRingBytes3;
+  static constexpr int STAGE_BYTES = 2 * kStageTokens * RB;
+  static constexpr int STAGES_RAW = RING_BYTES / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > kMaxStages ? kMaxStages : STAGES_RAW);
+  static_assert(WT % TPS == 0 && WT % TPV == 0 && PLT <= 32, "decode geometry");
+  static_assert(D % LPT == 0 && LB % VEC == 0, "head_dim");
 };
 
-// Shared-memory header in front of the stage ring (stage ring starts at 128-byte alignment).
+// Shared-memory header in front of the stage ring (the ring starts 128-byte aligned).
 struct DecodeSmemHeader {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
-  int32_t bad;    // set when a page id was out of range or a wait gave up
-  int32_t last;   // set in the CTA that merges the splits of its (row, kv head)
-  float p[kDecodeWarps][8][8];  // softmax weights of one step: [warp][token][head]
+  uint64_t full[kMaxStages];   // stage landed (bulk-copy bytes)
+  int32_t done[kMaxStages];    // warps finished with the stage; the last one refills it
+  int32_t bad;                 // a page id was out of range or a wait gave up
+  int32_t last;                // this CTA merges the splits of its (row, kv head)
+  int32_t issued;              // stages issued so far
+  int32_t pid[kMaxUnitPages];  // the unit's physical page ids
+  alignas(16) float p[kDecodeWarps][kStageTokens / kDecodeWarps][8];  // softmax weights: [warp][token][head]
 };
 
 __host__ __device__ constexpr size_t decode_header_bytes() { return (sizeof(DecodeSmemHeader) + 127) / 128 * 128; }
@@ -145,6 +170,27 @@ __device__ __forceinline__ void load_widen(const unsigned char* src, float* f) {
   }
 }
 
+// The G softmax weights of one token from the warp's exchange buffer (a broadcast read).
+template <int G>
+__device__ __forceinline__ void load_p(const float* src, float (&pv)[G]) {
+  if constexpr (G == 1) {
+    pv[0] = src[0];
+  } else if constexpr (G == 2) {
+    const float2 a = *reinterpret_cast<const float2*>(src);
+    pv[0] = a.x;
+    pv[1] = a.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < (G + 3) / 4; ++i) {
+      const float4 a = *reinterpret_cast<const float4*>(src + 4 * i);
+      if (4 * i < G) pv[4 * i] = a.x;
+      if (4 * i + 1 < G) pv[4 * i + 1] = a.y;
+      if (4 * i + 2 < G) pv[4 * i + 2] = a.z;
+      if (4 * i + 3 < G) pv[4 * i + 3] = a.w;
+    }
+  }
+}
+
 __device__ __forceinline__ float load_q(const void* q, bool bf16, size_t i) {
   if (bf16) return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(q)[i]) << 16);
   return reinterpret_cast<const float*>(q)[i];
@@ -163,13 +209,41 @@ __device__ __forceinline__ bool row_in_chunk(const AttnParams& p, int row) {
   return false;
 }
 
+// Copy the valid token slots of stage n (tokens t_begin + 32n .. +32, clipped
+// to t_end) into its ring slot: one bulk copy of K and one of V per page piece.
+template <int RB>
+__device__ __forceinline__ void issue_stage(const AttnParams& p, DecodeSmemHeader* hdr, unsigned char* ring, int n,
+                                            int nst, int t_begin, int t_end, int j0, int h, uint64_t policy) {
+  const int s = n % nst;
+  const int a = t_begin + n * kStageTokens;
+  const int b = min(t_end, a + kStageTokens);
+  unsigned char* ks = ring + static_cast<size_t>(s) * 2 * kStageTokens * RB;
+  unsigned char* vs = ks + kStageTokens * RB;
+  const size_t head_bytes = static_cast<size_t>(p.P) * RB;
+  const size_t page_bytes = head_bytes * p.Hkv;
+  const unsigned char* kb = reinterpret_cast<const unsigned char*>(p.k_pool) + h * head_bytes;
+  const unsigned char* vb = reinterpret_cast<const unsigned char*>(p.v_pool) + h * head_bytes;
+  mbar_arrive_expect_tx(&hdr->full[s], static_cast<uint32_t>(2 * (b - a) * RB));
+  for (int t = a; t < b;) {
+    const int page = hdr->pid[t / p.P - j0];
+    const int slot = t % p.P;
+    const int cnt = min(p.P - slot, b - t);
+    const size_t src = static_cast<size_t>(page) * page_bytes + static_cast<size_t>(slot) * RB;
+    const size_t dst = static_cast<size_t>(t - a) * RB;
+    bulk_g2s(ks + dst, kb + src, static_cast<uint32_t>(cnt * RB), &hdr->full[s], policy);
+    bulk_g2s(vs + dst, vb + src, static_cast<uint32_t>(cnt * RB), &hdr->full[s], policy);
+    t += cnt;
+  }
+}
+
 // ------------------------------------------------------------ the unit --
 
 template <int D, int G, int KVT>
 __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsigned char* smem) {
   using Geo = DecodeGeom<D, G, KVT>;
-  constexpr int NW = Geo::NW, LPT = Geo::LPT, TPS = Geo::TPS, NV = Geo::NV, EPV = Geo::EPV;
-  constexpr int DPL = Geo::DPL, RB = Geo::RB;
+  constexpr int NW = Geo::NW, LPT = Geo::LPT, TPS = Geo::TPS, U = Geo::U, NV = Geo::NV, EPV = Geo::EPV;
+  constexpr int PE = Geo::PE, PLT = Geo::PLT, TPV = Geo::TPV, NPV = Geo::NPV, RB = Geo::RB, WT = Geo::WT;
+  constexpr int ST = kStageTokens;
 
   const int h = unit % p.Hkv;
   const int rest = unit / p.Hkv;
@@ -200,213 +274,221 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
   const int t_begin = split * p.split_tokens;
   const int t_end = min(L, t_begin + p.split_tokens);
   const int j0 = t_begin / P;
-  const int npages = (t_end + P - 1) / P - j0;
+  const int npg = (t_end + P - 1) / P - j0;
+  const int nstage = (t_end - t_begin + ST - 1) / ST;
   const int nst = p.n_stages;
-  const uint32_t page_bytes = static_cast<uint32_t>(P) * RB;
 
   DecodeSmemHeader* hdr = reinterpret_cast<DecodeSmemHeader*>(smem);
-  unsigned char* stages = smem + decode_header_bytes();
+  unsigned char* ring = smem + decode_header_bytes();
   if (tid == 0) {
     for (int s = 0; s < nst; ++s) {
       mbar_init(&hdr->full[s], 1);
-      mbar_init(&hdr->empty[s], NW);
+      hdr->done[s] = 0;
     }
     hdr->bad = 0;
     hdr->last = 0;
+    hdr->issued = 0;
     fence_barrier_init();
   }
+  {
+    // the unit's page ids, range-checked before any copy
+    const int32_t* bt = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + j0;
+    bool bad = false;
+    for (int i = tid; i < npg && i < kMaxUnitPages; i += blockDim.x) {
+      const int pid = __ldg(bt + i);
+      bad |= pid < 0 || pid >= p.num_pages;
+      hdr->pid[i] = pid;
+    }
+    __syncthreads();  // barrier init and zeroed flags visible before the error flag is raised
+    if (bad) {
+      hdr->bad = 1;
+      record_error(p.status, ST_OUT_OF_RANGE);
+    }
+  }
   __syncthreads();
+  const bool unit_bad = hdr->bad != 0;
+  const uint64_t policy = l2_policy_evict_first();
+  if (tid == 0 && !unit_bad) {
+    const int first = min(nst, nstage);
+    for (int n = 0; n < first; ++n) issue_stage<RB>(p, hdr, ring, n, nst, t_begin, t_end, j0, h, policy);
+    hdr->issued = first;
+  }
 
-  const size_t head_stride = static_cast<size_t>(P) * RB;  // bytes of one (page, kv head)
-  const unsigned char* kbase = reinterpret_cast<const unsigned char*>(p.k_pool) + static_cast<size_t>(h) * head_stride;
-  const unsigned char* vbase = reinterpret_cast<const unsigned char*>(p.v_pool) + static_cast<size_t>(h) * head_stride;
-  const size_t page_stride = head_stride * p.Hkv;
-
-  float m_run[G], l_run[G], acc[G][DPL];
-
-  if (warp == NW) {
-    // ------------------------------------------------------------ producer
-    const uint64_t policy = l2_policy_evict_first();
-    const int32_t* bt = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
-    int issued = 0;
-    bool ok = true;
-    for (int nb = 0; nb < npages && ok; nb += 32) {
-      const int n_mine = nb + lane;
-      int pid = 0;
-      bool bad = false;
-      if (n_mine < npages) {
-        pid = __ldg(bt + j0 + n_mine);
-        bad = pid < 0 || pid >= p.num_pages;
+  // ---- per-warp state
+  float m_ref[G], l_run[G], acc[G][PE];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m_ref[g] = -INFINITY;
+    l_run[g] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < PE; ++e) acc[g][e] = 0.0f;
+  }
+  const int tok = lane / LPT;   // QK: token of this lane within a sub-step
+  const int part = lane % LPT;  // QK: which slice of the row
+  // Query slice in registers, pre-scaled into the log2 domain.  Load i of a
+  // lane reads vector part + LPT * ((i + tok) % NV) of the row: rotating by
+  // the token spreads one sub-step's tokens over all shared-memory banks.
+  float qr[G][NV][EPV];
+  {
+    const size_t qrow = (static_cast<size_t>(row) * p.Hq + static_cast<size_t>(h) * G) * D;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int vidx = part + LPT * ((i + tok) % NV);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e)
+          qr[g][i][e] =
+              __fmul_rn(load_q(p.q, q_bf16, qrow + static_cast<size_t>(g) * D + vidx * EPV + e), p.qk_scale_log2);
       }
-      const unsigned bad_mask = __ballot_sync(0xffffffffu, bad);
-      const int cnt = min(32, npages - nb);
-      for (int k = 0; k < cnt; ++k) {
-        const int page = __shfl_sync(0xffffffffu, pid, k);
-        const int n = nb + k;
-        const int s = n % nst, r = n / nst;
-        if (lane == 0) {
-          if (r > 0 && !mbar_wait(&hdr->empty[s], (r - 1) & 1, p.wait_limit)) {
-            record_error(p.status, ST_TIMEOUT);
-            hdr->bad = 1;
-            ok = false;
-          } else if ((bad_mask >> k) & 1u) {
-            record_error(p.status, ST_OUT_OF_RANGE);
-            hdr->bad = 1;
-            mbar_arrive(&hdr->full[s]);  // completes the phase with no data
-          } else {
-            const int first_tok = (j0 + n) * P;
-            const int valid = min(P, t_end - first_tok);
-            const uint32_t bytes = static_cast<uint32_t>(valid) * RB;
-            unsigned char* ks = stages + static_cast<size_t>(s) * 2 * page_bytes;
-            mbar_arrive_expect_tx(&hdr->full[s], 2 * bytes);
-            bulk_g2s(ks, kbase + static_cast<size_t>(page) * page_stride, bytes, &hdr->full[s], policy);
-            bulk_g2s(ks + page_bytes, vbase + static_cast<size_t>(page) * page_stride, bytes, &hdr->full[s], policy);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        issued = n + 1;
-      }
-    }
-    // Every issued copy must land before this CTA's shared memory is reused.
-    if (lane == 0)
-      for (int n = max(0, issued - nst); n < issued; ++n) mbar_wait(&hdr->full[n % nst], (n / nst) & 1, kDrainWaitLimit);
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int tok = lane / LPT;   // token of this lane within a step
-    const int part = lane % LPT;  // which slice of the row
-    // Query slice in registers, pre-scaled into the log2 domain.  Load i of
-    // token tok reads vector part + LPT * ((i + tok) % NV) of the row: the
-    // rotation by tok spreads one step's tokens over all shared-memory banks.
-    float qr[G][NV][EPV];
-    {
-      const size_t qrow = (static_cast<size_t>(row) * p.Hq + static_cast<size_t>(h) * G) * D;
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-          const int vidx = part + LPT * ((i + tok) % NV);
-#pragma unroll
-          for (int e = 0; e < EPV; ++e)
-            qr[g][i][e] = __fmul_rn(load_q(p.q, q_bf16, qrow + static_cast<size_t>(g) * D + vidx * EPV + e), p.qk_scale_log2);
-        }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m_run[g] = -INFINITY;
-      l_run[g] = 0.0f;
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) acc[g][e] = 0.0f;
-    }
-    const int steps_per_page = P / TPS;
-    float* pbuf = &hdr->p[warp][0][0];
+  }
+  float* pbuf = &hdr->p[warp][0][0];
+  const int pv_tok = lane / PLT;           // P.V: token of this lane within an iteration
+  const int pv_off = (lane % PLT) * Geo::VB;  // P.V: byte offset of this lane's elements
 
-    for (int n = 0; n < npages; ++n) {
-      const int s = n % nst, r = n / nst;
-      const bool landed = __all_sync(0xffffffffu, mbar_wait(&hdr->full[s], r & 1, p.wait_limit));
-      if (!landed) {
-        if (lane == 0) {
-          record_error(p.status, ST_TIMEOUT);
-          hdr->bad = 1;
-        }
-        break;
+  for (int n = 0; n < nstage && !unit_bad; ++n) {
+    const int s = n % nst;
+    const bool landed = __all_sync(0xffffffffu, mbar_wait(&hdr->full[s], (n / nst) & 1, p.wait_limit));
+    if (!landed) {
+      if (lane == 0) {
+        record_error(p.status, ST_TIMEOUT);
+        hdr->bad = 1;
       }
-      const unsigned char* ks = stages + static_cast<size_t>(s) * 2 * page_bytes;
-      const unsigned char* vs = ks + page_bytes;
-      const int page_tok0 = (j0 + n) * P;
-      for (int k = 0; k < steps_per_page; ++k) {
-        if ((n * steps_per_page + k) % NW != warp) continue;
-        const int t0 = page_tok0 + k * TPS;
-        const int n_valid = min(TPS, t_end - t0);
-        if (n_valid <= 0) break;
-        // ---- scores of this step's tokens (log2 domain)
-        float sc[G];
+      break;
+    }
+    const unsigned char* ks = ring + static_cast<size_t>(s) * 2 * ST * RB;
+    const unsigned char* vs = ks + ST * RB;
+    const int wtok0 = warp * WT;  // this warp's first token in the stage
+    const int n_valid = min(WT, t_end - (t_begin + n * ST + wtok0));
+    if (n_valid > 0) {
+      // ---- scores of the warp's WT tokens (log2 domain), U sub-steps of TPS tokens
+      float sc[U][G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) sc[g] = 0.0f;
-        const unsigned char* krow = ks + static_cast<size_t>(k * TPS + tok) * RB;
+      for (int u = 0; u < U; ++u) {
+        const unsigned char* krow = ks + static_cast<size_t>(wtok0 + u * TPS + tok) * RB;
+        float partial[G][NV];
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
           const int vidx = part + LPT * ((i + tok) % NV);
           float kf[EPV];
           load_widen<KVT, Geo::VEC>(krow + vidx * Geo::VEC, kf);
 #pragma unroll
-          for (int g = 0; g < G; ++g)
+          for (int g = 0; g < G; ++g) {
+            float a = __fmul_rn(qr[g][i][0], kf[0]);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) sc[g] = fmaf(qr[g][i][e], kf[e], sc[g]);
+            for (int e = 1; e < EPV; ++e) a = fmaf(qr[g][i][e], kf[e], a);
+            partial[g][i] = a;
+          }
         }
-#pragma unroll
-        for (int off = 1; off < LPT; off <<= 1)
-#pragma unroll
-          for (int g = 0; g < G; ++g) sc[g] = __fadd_rn(sc[g], __shfl_xor_sync(0xffffffffu, sc[g], off));
-        const bool valid = tok < n_valid;
-        // ---- online softmax update (m is the same in every lane of the warp)
-        float pw[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          if (!valid) sc[g] = -INFINITY;
-          float mx = sc[g];
+          float a = partial[g][0];
 #pragma unroll
-          for (int off = LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          if (mx > m_run[g]) {
-            const float alpha = exp2f(__fsub_rn(m_run[g], mx));
-            m_run[g] = mx;
-            l_run[g] = __fmul_rn(l_run[g], alpha);
+          for (int i = 1; i < NV; ++i) a = __fadd_rn(a, partial[g][i]);
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[g][e] = __fmul_rn(acc[g][e], alpha);
-          }
-          pw[g] = valid ? exp2f(__fsub_rn(sc[g], m_run[g])) : 0.0f;
-          l_run[g] = __fadd_rn(l_run[g], pw[g]);
+          for (int off = 1; off < LPT; off <<= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, off));
+          sc[u][g] = (u * TPS + tok < n_valid) ? a : -INFINITY;
         }
-        __syncwarp();
-        if (part == 0) {
+      }
+      // ---- online softmax: one reference-max update per stage.  The reference
+      // only moves when the new maximum exceeds it by more than kRescaleSlack
+      // (log2 units), so weights stay <= 2^kRescaleSlack and rescaling is rare.
 #pragma unroll
-          for (int g = 0; g < G; ++g) pbuf[tok * 8 + g] = pw[g];
+      for (int g = 0; g < G; ++g) {
+        float mx = sc[0][g];
+#pragma unroll
+        for (int u = 1; u < U; ++u) mx = fmaxf(mx, sc[u][g]);
+#pragma unroll
+        for (int off = LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (mx > __fadd_rn(m_ref[g], kRescaleSlack)) {
+          const float alpha = ex2(__fsub_rn(m_ref[g], mx));
+          m_ref[g] = mx;
+          l_run[g] = __fmul_rn(l_run[g], alpha);
+#pragma unroll
+          for (int e = 0; e < PE; ++e) acc[g][e] = __fmul_rn(acc[g][e], alpha);
         }
-        __syncwarp();
-        // ---- acc += p . V over the step's valid tokens, in token order
-        const unsigned char* vrow = vs + static_cast<size_t>(k * TPS) * RB + lane * Geo::VB;
-        for (int tt = 0; tt < n_valid; ++tt) {
-          float vf[DPL];
-          load_widen<KVT, Geo::VB>(vrow + static_cast<size_t>(tt) * RB, vf);
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float pv = pbuf[tt * 8 + g];
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[g][e] = fmaf(pv, vf[e], acc[g][e]);
-          }
+        for (int u = 0; u < U; ++u) {  // scores become weights in place
+          sc[u][g] = (u * TPS + tok < n_valid) ? ex2(__fsub_rn(sc[u][g], m_ref[g])) : 0.0f;
+          l_run[g] = __fadd_rn(l_run[g], sc[u][g]);
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&hdr->empty[s]);
+      if (part == 0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int g = 0; g < G; ++g) pbuf[(u * TPS + tok) * 8 + g] = sc[u][g];
+      }
+      __syncwarp();
+      // ---- acc += p . V over the warp's valid tokens, TPV tokens per iteration
+#pragma unroll
+      for (int it = 0; it < NPV; ++it) {
+        const int t = it * TPV + pv_tok;
+        if (t < n_valid) {
+          float vf[PE];
+          load_widen<KVT, Geo::VB>(vs + static_cast<size_t>(wtok0 + t) * RB + pv_off, vf);
+          float pv[G];
+          load_p<G>(pbuf + t * 8, pv);
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < PE; ++e) acc[g][e] = fmaf(pv[g], vf[e], acc[g][e]);
+        }
+      }
     }
-    // each lane summed only its own token's weights: add over the token lanes
+    // ---- release the stage; the last warp to finish refills it
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&hdr->done[s], 1) == NW - 1) {
+        hdr->done[s] = 0;
+        const int nn = n + nst;
+        if (nn < nstage) {
+          fence_proxy_async();
+          issue_stage<RB>(p, hdr, ring, nn, nst, t_begin, t_end, j0, h, policy);
+          atomicMax(&hdr->issued, nn + 1);
+        }
+      }
+    }
+  }
+  // each lane summed only its own tokens: complete l over the token lanes and
+  // acc over the P.V token groups (fixed xor trees)
 #pragma unroll
-    for (int off = LPT; off < 32; off <<= 1)
+  for (int g = 0; g < G; ++g) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) l_run[g] = __fadd_rn(l_run[g], __shfl_xor_sync(0xffffffffu, l_run[g], off));
+    for (int off = LPT; off < 32; off <<= 1) l_run[g] = __fadd_rn(l_run[g], __shfl_xor_sync(0xffffffffu, l_run[g], off));
+#pragma unroll
+    for (int e = 0; e < PE; ++e)
+#pragma unroll
+      for (int off = PLT; off < 32; off <<= 1) acc[g][e] = __fadd_rn(acc[g][e], __shfl_xor_sync(0xffffffffu, acc[g][e], off));
   }
 
-  __syncthreads();  // all copies landed and consumed: the stage ring is free
+  __syncthreads();
+  if (tid == 0) {
+    // every issued copy must land before the ring is reused (only matters after a timeout)
+    const int issued = hdr->issued;
+    for (int n = max(0, issued - nst); n < issued; ++n) mbar_wait(&hdr->full[n % nst], (n / nst) & 1, kDrainWaitLimit);
+  }
+  __syncthreads();
 
-  // ---- merge the 4 consumer warps' states, warp 0 first
-  float* red_acc = reinterpret_cast<float*>(stages);      // [NW][G][D]
-  float* red_ml = red_acc + NW * G * D;                   // [NW][G][2]
-  if (warp < NW) {
+  // ---- merge the 4 warps' states, warp 0 first
+  float* red_acc = reinterpret_cast<float*>(ring);  // [NW][G][D]
+  float* red_ml = red_acc + NW * G * D;             // [NW][G][2]
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
+  for (int g = 0; g < G; ++g) {
+    if (lane < PLT) {
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) red_acc[(warp * G + g) * D + lane * DPL + e] = acc[g][e];
-      if (lane == 0) {
-        red_ml[(warp * G + g) * 2] = m_run[g];
-        red_ml[(warp * G + g) * 2 + 1] = l_run[g];
-      }
+      for (int e = 0; e < PE; ++e) red_acc[(warp * G + g) * D + lane * PE + e] = acc[g][e];
+    }
+    if (lane == 0) {
+      red_ml[(warp * G + g) * 2] = m_ref[g];
+      red_ml[(warp * G + g) * 2 + 1] = l_run[g];
     }
   }
   __syncthreads();
   const bool bad = hdr->bad != 0;
   const size_t out_row = static_cast<size_t>(row) * p.Hq + static_cast<size_t>(h) * G;
-
   if (nsplit == 1) {
     for (int i = tid; i < G * D; i += blockDim.x) {
       const int g = i / D, d = i % D;
@@ -416,7 +498,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
       float lsum = 0.0f, osum = 0.0f;
 #pragma unroll
       for (int w = 0; w < NW; ++w) {
-        const float f = exp2f(__fsub_rn(red_ml[(w * G + g) * 2], M));
+        const float f = ex2(__fsub_rn(red_ml[(w * G + g) * 2], M));
         lsum = fmaf(f, red_ml[(w * G + g) * 2 + 1], lsum);
         osum = fmaf(f, red_acc[(w * G + g) * D + d], osum);
       }
@@ -436,7 +518,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
     float lsum = 0.0f, osum = 0.0f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const float f = exp2f(__fsub_rn(red_ml[(w * G + g) * 2], M));
+      const float f = ex2(__fsub_rn(red_ml[(w * G + g) * 2], M));
       lsum = fmaf(f, red_ml[(w * G + g) * 2 + 1], lsum);
       osum = fmaf(f, red_acc[(w * G + g) * D + d], osum);
     }
@@ -466,7 +548,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
     for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(p.ws_ml + (slot0 + sp) * 2));
     float lsum = 0.0f, osum = 0.0f;
     for (int sp = 0; sp < nsplit; ++sp) {
-      const float f = exp2f(__fsub_rn(__ldcg(p.ws_ml + (slot0 + sp) * 2), M));
+      const float f = ex2(__fsub_rn(__ldcg(p.ws_ml + (slot0 + sp) * 2), M));
       lsum = fmaf(f, __ldcg(p.ws_ml + (slot0 + sp) * 2 + 1), lsum);
       osum = fmaf(f, __ldcg(p.ws_o + (slot0 + sp) * D + d), osum);
     }
@@ -478,7 +560,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
 }
 
 template <int D, int G, int KVT>
-__global__ void __launch_bounds__(DecodeGeom<D, G, KVT>::THREADS, 3) decode_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(DecodeGeom<D, G, KVT>::THREADS, DecodeGeom<D, G, KVT>::MIN_CTAS) decode_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   decode_unit<D, G, KVT>(p, static_cast<int>(blockIdx.x) - p.n_prefill_ctas, smem);
 }
@@ -486,13 +568,17 @@ __global__ void __launch_bounds__(DecodeGeom<D, G, KVT>::THREADS, 3) decode_kern
 template <int D, int G, int KVT>
 size_t decode_smem_for(int P, int n_stages) {
   using Geo = DecodeGeom<D, G, KVT>;
-  const size_t ring = static_cast<size_t>(n_stages) * 2 * P * Geo::RB;
+  (void)P;
+  const size_t ring = static_cast<size_t>(n_stages) * 2 * kStageTokens * Geo::RB;
   const size_t merge = static_cast<size_t>(Geo::NW) * G * (D + 2) * sizeof(float);
   return decode_header_bytes() + (ring > merge ? ring : merge);
 }
 
 template <int D, int G, int KVT>
-cudaError_t launch_decode_inst(const AttnParams& p, cudaStream_t stream) {
+cudaError_t launch_decode_inst(const AttnParams& p0, cudaStream_t stream) {
+  using Geo = DecodeGeom<D, G, KVT>;
+  AttnParams p = p0;
+  p.n_stages = Geo::STAGES;
   const size_t smem = decode_smem_for<D, G, KVT>(p.P, p.n_stages);
   static int attr_bytes = 0;  // largest dynamic shared memory size already allowed
   if (static_cast<int>(smem) > attr_bytes) {
@@ -503,7 +589,7 @@ cudaError_t launch_decode_inst(const AttnParams& p, cudaStream_t stream) {
   }
   const long long units = static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
   if (units <= 0) return cudaSuccess;
-  decode_kernel<D, G, KVT><<<static_cast<unsigned>(units), DecodeGeom<D, G, KVT>::THREADS, smem, stream>>>(p);
+  decode_kernel<D, G, KVT><<<static_cast<unsigned>(units), Geo::THREADS, smem, stream>>>(p);
   count_launch();
   return cudaGetLastError();
 }
@@ -531,30 +617,6 @@ cudaError_t launch_decode_dispatch(const AttnParams& p, cudaStream_t stream) {
   PA_DECODE_CASE(64, 8)
 #undef PA_DECODE_CASE
   return cudaErrorNotSupported;
-}
-
-template <int KVT>
-size_t decode_smem_dispatch(int P, int D, int G, int n_stages) {
-#define PA_SMEM_CASE(DD, GG) \
-  if (D == DD && G == GG) return decode_smem_for<DD, GG, KVT>(P, n_stages);
-  PA_SMEM_CASE(128, 1)
-  PA_SMEM_CASE(128, 2)
-  PA_SMEM_CASE(128, 3)
-  PA_SMEM_CASE(128, 4)
-  PA_SMEM_CASE(128, 5)
-  PA_SMEM_CASE(128, 6)
-  PA_SMEM_CASE(128, 7)
-  PA_SMEM_CASE(128, 8)
-  PA_SMEM_CASE(64, 1)
-  PA_SMEM_CASE(64, 2)
-  PA_SMEM_CASE(64, 3)
-  PA_SMEM_CASE(64, 4)
-  PA_SMEM_CASE(64, 5)
-  PA_SMEM_CASE(64, 6)
-  PA_SMEM_CASE(64, 7)
-  PA_SMEM_CASE(64, 8)
-#undef PA_SMEM_CASE
-  return 0;
 }
 
 }  // namespace pa

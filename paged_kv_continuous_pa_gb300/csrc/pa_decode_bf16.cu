@@ -8,8 +8,5 @@ cudaError_t launch_decode_bf16(const AttnParams& p, cudaStream_t stream) {
   return launch_decode_dispatch<KV_BF16>(p, stream);
 }
 
-size_t decode_smem_bytes_bf16(int P, int D, int G, int n_stages) {
-  return decode_smem_dispatch<KV_BF16>(P, D, G, n_stages);
-}
 
 }  // namespace pa

@@ -92,6 +92,19 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
+// Order this thread's generic-proxy shared-memory accesses before its later
+// async-proxy (bulk-copy) operations on shared memory.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 2^x with the hardware approximation (ex2.approx.ftz.f32: relative error
+// about 2^-22, subnormal results flushed to zero).  Softmax weights below
+// 2^-126 contribute nothing at FP32 precision.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------ conversions --
 
 // Two bf16 packed in a 32-bit word -> two floats (exact).

@@ -8,11 +8,28 @@
 namespace pa {
 
 constexpr int kMaxChunks = 16;          // prefill chunks per pa_attention call
-constexpr int kDefaultSplitTokens = 1024;
+constexpr int kDefaultSplitTokens = 4096;
 constexpr uint32_t kDefaultWaitLimit = 1u << 22;  // polls of one bounded wait (about a second)
 constexpr uint32_t kDrainWaitLimit = 1u << 22;    // polls spent draining copies on an error path
 constexpr int kMaxStages = 16;          // decode pipeline depth upper bound
-constexpr int kDecodeWarps = 4;         // consumer warps of a decode CTA (+1 producer warp)
+constexpr int kDecodeWarps = 4;         // warps of a decode CTA
+constexpr int kStageTokens = 32;        // tokens per decode pipeline stage
+constexpr int kMaxUnitPages = 256;      // page ids a decode unit caches (split_tokens <= 256 * 16)
+constexpr int kMaxSplitTokens = 4096;
+constexpr float kRescaleSlack = 8.0f;   // log2-domain headroom before the running max is moved
+
+// Decode occupancy target and the stage-ring budget that goes with it: the
+// ring is sized so that kDecodeMinCtas CTAs fit in an SM's shared memory, and
+// registers are capped so that they fit in its register file.
+#ifndef PA_DECODE_MIN_CTAS
+#define PA_DECODE_MIN_CTAS 4
+#endif
+#ifndef PA_DECODE_RING_KB
+#define PA_DECODE_RING_KB 48
+#endif
+constexpr int kDecodeMinCtas = PA_DECODE_MIN_CTAS;
+constexpr int kDecodeRingBytes = PA_DECODE_RING_KB * 1024;   // at four CTAs per SM
+constexpr int kDecodeRingBytes3 = 64 * 1024;                 // at three CTAs per SM
 
 enum KvType { KV_F32 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
 
@@ -55,7 +72,7 @@ struct AttnParams {
   int32_t* ws_count;     // [n_rows][Hkv] finished-split counters, zero between calls
   int32_t* status;
   uint32_t wait_limit;
-  int32_t n_stages;      // decode pipeline depth
+  int32_t n_stages;      // decode pipeline depth (set per instantiation at launch)
   int32_t n_prefill_ctas;  // CTAs [0, n_prefill_ctas) run prefill tiles, the rest decode units
   int32_t n_chunks;
   int32_t chunk_begin[kMaxChunks];
@@ -76,9 +93,5 @@ cudaError_t launch_decode_f32(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_decode_e4m3(const AttnParams& p, cudaStream_t stream);
 
-// Dynamic shared memory a decode CTA needs for this geometry (0 = no instantiation).
-size_t decode_smem_bytes_f32(int P, int D, int G, int n_stages);
-size_t decode_smem_bytes_bf16(int P, int D, int G, int n_stages);
-size_t decode_smem_bytes_e4m3(int P, int D, int G, int n_stages);
 
 }  // namespace pa

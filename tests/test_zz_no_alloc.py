@@ -32,7 +32,16 @@ def _noalloc_raw(lib, st, q, seq, pos, out):
 def test_noalloc_matches_workspace_entry_point_twice():
     pa_build.build()
     lib = pa.load()
-    wl = W.batched_decode(n_seqs=40, ctx_lo=900)  # every row is split at 1024-token splits or close to it
+    old_split = pa.get_split_tokens()
+    pa.set_split_tokens(1024)  # so that the rows are split and the scratch is used
+    try:
+        _compare_twice(lib)
+    finally:
+        pa.set_split_tokens(old_split)
+
+
+def _compare_twice(lib):
+    wl = W.batched_decode(n_seqs=40, ctx_lo=900)
     st = pa_setup.upload(wl)
     st.append_step()
     torch.cuda.synchronize()
