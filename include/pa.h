@@ -120,11 +120,13 @@ pa_status pa_append_kv(const pa_pool *pool, int32_t n_rows, const void *k_new, c
                        const int32_t *block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
                        int32_t *status_dev, void *stream);
 
-/* Workspace bytes pa_attention needs for this many rows and this block-table
- * width (the split-KV partial triples and their per-(row, kv head) counters).
- * 0 when no row can be split.  Computed on the host from sizes only. */
+/* Workspace bytes pa_attention needs for these rows, this block-table width
+ * and these prefill chunks (the split-KV partial triples of decode rows and of
+ * chunk tiles, and their counters).  0 when nothing can be split.  Computed on
+ * the host from sizes only; for a bf16 pool it assumes the chunks take the
+ * tensor-core tile path (bf16 queries), which never needs less. */
 size_t pa_attention_workspace_bytes(const pa_pool *pool, int32_t n_rows, int32_t num_q_heads,
-                                    int32_t max_blocks_per_seq);
+                                    int32_t max_blocks_per_seq, const pa_chunk *chunks, int32_t n_chunks);
 
 /* Paged attention over a step's rows (see the top of this file).
  *   q_dtype      PA_F32 or PA_BF16; out has the same dtype, rounded to nearest even
@@ -184,6 +186,14 @@ int32_t pa_get_split_tokens(void);
  * knob: with 1, waits give up almost at once, which exercises the error path
  * without any real hang. */
 void pa_set_wait_limit(uint32_t polls);
+
+/* Failure-path testing without a GPU fault: with enable != 0, every attention
+ * CTA additionally waits on a barrier that nothing ever completes, so that
+ * wait runs out after the current wait limit; the call then reports
+ * PA_ERR_TIMEOUT in *status_dev, its outputs are unspecified, and the kernel
+ * still returns normally.  Set a small wait limit first (e.g. 1000 polls).
+ * Off by default; affects calls made while it is on. */
+void pa_debug_stall_waits(int32_t enable);
 
 const char *pa_status_string(pa_status status);
 

@@ -83,7 +83,7 @@ def upload(wl: W.Workload, device="cuda", hist_batch_rows: int = 1 << 19) -> Dev
                      torch.from_numpy(wl.hist_seq[b:e]).to(device), torch.from_numpy(wl.hist_pos[b:e]).to(device),
                      bt, status=status)
     q = to_torch(wl.q, wl.q_dtype, device)
-    ws_bytes = pa.workspace_bytes(pool, wl.n_rows, wl.Hq, wl.max_blocks)
+    ws_bytes = pa.workspace_bytes(pool, wl.n_rows, wl.Hq, wl.max_blocks, wl.chunks)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device) if ws_bytes else None
     step = DeviceStep(wl=wl, pool=pool, k_pool=k_pool, v_pool=v_pool, block_tables=bt,
                       seq_ids=torch.from_numpy(wl.seq_ids).to(device),

@@ -66,7 +66,7 @@ def load(path: str = LIB_PATH):
         L.pa_pool_destroy.restype = None
         L.pa_append_kv.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, i32, i32, vp, vp]
         L.pa_append_kv.restype = st
-        L.pa_attention_workspace_bytes.argtypes = [vp, i32, i32, i32]
+        L.pa_attention_workspace_bytes.argtypes = [vp, i32, i32, i32, ctypes.POINTER(Chunk), i32]
         L.pa_attention_workspace_bytes.restype = sz
         L.pa_attention.argtypes = [vp, i32, vp, i32, i32, vp, vp, vp, i32, i32, ctypes.POINTER(Chunk), i32, f32, vp,
                                    vp, sz, vp, vp]
@@ -80,6 +80,8 @@ def load(path: str = LIB_PATH):
         L.pa_get_split_tokens.restype = i32
         L.pa_set_wait_limit.argtypes = [ctypes.c_uint32]
         L.pa_set_wait_limit.restype = None
+        L.pa_debug_stall_waits.argtypes = [i32]
+        L.pa_debug_stall_waits.restype = None
         L.pa_status_string.argtypes = [st]
         L.pa_status_string.restype = ctypes.c_char_p
         L.pa_last_error.argtypes = []
@@ -181,8 +183,11 @@ def append_kv(pool: Pool, k_new, v_new, seq_ids, positions, block_tables, status
                                _stream(stream)))
 
 
-def workspace_bytes(pool: Pool, n_rows: int, num_q_heads: int, max_blocks: int) -> int:
-    return int(load().pa_attention_workspace_bytes(pool.handle, int(n_rows), int(num_q_heads), int(max_blocks)))
+def workspace_bytes(pool: Pool, n_rows: int, num_q_heads: int, max_blocks: int,
+                    chunks: Sequence[Tuple[int, int]] = ()) -> int:
+    arr = (Chunk * max(1, len(chunks)))(*[Chunk(int(b), int(c)) for b, c in chunks])
+    return int(load().pa_attention_workspace_bytes(pool.handle, int(n_rows), int(num_q_heads), int(max_blocks),
+                                                   arr if chunks else None, len(chunks)))
 
 
 def attention(pool: Pool, q, seq_ids, positions, block_tables, out,
@@ -232,6 +237,10 @@ def set_wait_limit(polls: int):
 
 def kernel_launches() -> int:
     return int(load().pa_kernel_launches())
+
+
+def debug_stall_waits(enable: bool):
+    load().pa_debug_stall_waits(1 if enable else 0)
 
 
 def version() -> str:

@@ -7,6 +7,10 @@
 #include <cstring>
 #include <new>
 
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "../../include/pa.h"
 #include "pa_kernels.h"
 
@@ -14,6 +18,9 @@ struct pa_pool {
   pa_pool_desc desc;
   void* k;
   void* v;
+  bool maps_ready;   // kmap / vmap encoded (on first use by the tile path)
+  CUtensorMap kmap;  // 2-D views of the pools for tensor-map copies
+  CUtensorMap vmap;
 };
 
 namespace {
@@ -27,6 +34,7 @@ namespace {
 thread_local char g_last_error[512] = "";
 int32_t g_split_tokens = pa::kDefaultSplitTokens;
 uint32_t g_wait_limit = pa::kDefaultWaitLimit;
+int32_t g_debug_stall = 0;
 
 pa_status fail(pa_status st, const char* fmt, ...) {
   va_list ap;
@@ -49,21 +57,107 @@ int max_splits_for(const pa_pool_desc& d, int32_t max_blocks) {
   return static_cast<int>((cap + g_split_tokens - 1) / g_split_tokens);
 }
 
-// Workspace layout: [counters: n_rows*Hkv int32, padded to 256 B][ml: n_rows*Hq*S*2 f32][o: n_rows*Hq*S*D f32]
-struct WsLayout {
-  size_t count_off, ml_off, o_off, total;
+// How one pa_attention call is laid out: which chunks take the tensor-core
+// tile path, how many CTAs that takes, and where the split-KV partials live in
+// the caller's workspace.  Decided from host-known sizes only.
+struct Plan {
+  int G = 1, R = 0;
+  int max_splits = 1;     // decode splits per row
+  int tile_splits = 0;    // key-range splits per tile (0: no tile path)
+  int n_tile = 0;         // chunks on the tile path
+  int src[pa::kMaxChunks];
+  int cta_begin[pa::kMaxChunks + 1];
+  int row_begin[pa::kMaxChunks];
+  int tile_begin[pa::kMaxChunks];
+  int total_tiles = 0, total_rows = 0;
+  // workspace byte offsets
+  size_t d_count = 0, d_ml = 0, d_o = 0, t_count = 0, t_ml = 0, t_o = 0, total = 0;
 };
 
-WsLayout ws_layout(const pa_pool_desc& d, int32_t n_rows, int32_t hq, int max_splits) {
-  WsLayout w{0, 0, 0, 0};
-  if (max_splits <= 1 || n_rows <= 0) return w;
+Plan make_plan(const pa_pool_desc& d, int32_t n_rows, int32_t hq, int32_t max_blocks, const pa_chunk* chunks,
+               int32_t n_chunks, bool tile_dtypes) {
+  Plan pl;
+  pl.G = hq / d.num_kv_heads;
+  pl.max_splits = max_splits_for(d, max_blocks);
+  pl.R = pa::kTileRowsTotal / pl.G;
+  if (tile_dtypes && chunks != nullptr) {
+    const long long keys = static_cast<long long>(max_blocks) * d.page_size;
+    pl.tile_splits = static_cast<int>((keys + pa::kTileSplitKeys - 1) / pa::kTileSplitKeys);
+    int ctas = 0;
+    for (int c = 0; c < n_chunks && c < pa::kMaxChunks; ++c) {
+      if (chunks[c].n_rows < pa::kMinTileRows) continue;
+      const int k = pl.n_tile++;
+      const int n_mt = (chunks[c].n_rows + pl.R - 1) / pl.R;
+      pl.src[k] = c;
+      pl.cta_begin[k] = ctas;
+      pl.row_begin[k] = pl.total_rows;
+      pl.tile_begin[k] = pl.total_tiles;
+      ctas += d.num_kv_heads * n_mt * pl.tile_splits;
+      pl.total_rows += chunks[c].n_rows;
+      pl.total_tiles += d.num_kv_heads * n_mt;
+    }
+    pl.cta_begin[pl.n_tile] = ctas;
+    if (pl.n_tile == 0) pl.tile_splits = 0;
+  }
   auto pad = [](size_t x) { return (x + 255) / 256 * 256; };
-  const size_t slots = static_cast<size_t>(n_rows) * hq * max_splits;
-  w.count_off = 0;
-  w.ml_off = pad(static_cast<size_t>(n_rows) * d.num_kv_heads * sizeof(int32_t));
-  w.o_off = w.ml_off + pad(slots * 2 * sizeof(float));
-  w.total = w.o_off + pad(slots * d.head_dim * sizeof(float));
-  return w;
+  size_t off = 0;
+  if (pl.max_splits > 1 && n_rows > 0) {
+    const size_t slots = static_cast<size_t>(n_rows) * hq * pl.max_splits;
+    pl.d_count = off;
+    off += pad(static_cast<size_t>(n_rows) * d.num_kv_heads * sizeof(int32_t));
+    pl.d_ml = off;
+    off += pad(slots * 2 * sizeof(float));
+    pl.d_o = off;
+    off += pad(slots * d.head_dim * sizeof(float));
+  }
+  if (pl.tile_splits > 1) {
+    const size_t slots = static_cast<size_t>(pl.total_rows) * hq * pl.tile_splits;
+    pl.t_count = off;
+    off += pad(static_cast<size_t>(pl.total_tiles) * sizeof(int32_t));
+    pl.t_ml = off;
+    off += pad(slots * 2 * sizeof(float));
+    pl.t_o = off;
+    off += pad(slots * d.head_dim * sizeof(float));
+  }
+  pl.total = off;
+  return pl;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// The pool as a 2-D bf16 tensor [num_pages * Hkv * P rows][D], boxes of 64
+// elements x P rows (one page of one kv head, half or all of the head dim),
+// 128-byte swizzle: the layout the tensor-core tile path reads.
+pa_status encode_pool_maps(pa_pool* pool) {
+  if (pool->maps_ready) return PA_OK;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const pa_pool_desc& d = pool->desc;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim),
+                        static_cast<cuuint64_t>(d.num_pages) * d.num_kv_heads * d.page_size};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(d.page_size)};
+  cuuint32_t estr[2] = {1, 1};
+  for (int i = 0; i < 2; ++i) {
+    CUresult r = enc(i == 0 ? &pool->kmap : &pool->vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, i == 0 ? pool->k : pool->v,
+                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  }
+  pool->maps_ready = true;
+  return PA_OK;
 }
 
 pa_status check_desc(const pa_pool_desc* d) {
@@ -113,6 +207,7 @@ pa_status pa_pool_create(const pa_pool_desc* desc, void* k_pool, void* v_pool, p
   if (p->desc.kv_dtype != PA_FP8_E4M3) p->desc.k_scale = p->desc.v_scale = 1.0f;
   p->k = k_pool;
   p->v = v_pool;
+  p->maps_ready = false;
   *out = p;
   return PA_OK;
 }
@@ -158,9 +253,14 @@ pa_status pa_append_kv(const pa_pool* pool, int32_t n_rows, const void* k_new, c
 }
 
 size_t pa_attention_workspace_bytes(const pa_pool* pool, int32_t n_rows, int32_t num_q_heads,
-                                    int32_t max_blocks_per_seq) {
-  if (pool == nullptr || n_rows <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0) return 0;
-  return ws_layout(pool->desc, n_rows, num_q_heads, max_splits_for(pool->desc, max_blocks_per_seq)).total;
+                                    int32_t max_blocks_per_seq, const pa_chunk* chunks, int32_t n_chunks) {
+  if (pool == nullptr || n_rows <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 ||
+      num_q_heads % pool->desc.num_kv_heads != 0 || n_chunks < 0)
+    return 0;
+  // chunks of a bf16 pool may take the tile path (with bf16 queries): size for it
+  return make_plan(pool->desc, n_rows, num_q_heads, max_blocks_per_seq, chunks, n_chunks,
+                   pool->desc.kv_dtype == PA_BF16)
+      .total;
 }
 
 pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dtype q_dtype, int32_t num_q_heads,
@@ -195,11 +295,11 @@ pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dt
   if (n_rows == 0) return PA_OK;
   if (!q || !seq_ids || !positions || !block_tables || !out)
     return fail(PA_ERR_INVALID_ARG, "attention: a device pointer is NULL");
-  const int max_splits = max_splits_for(d, max_blocks_per_seq);
-  const WsLayout ws = ws_layout(d, n_rows, num_q_heads, max_splits);
-  if (ws.total > 0) {
-    if (workspace == nullptr || workspace_bytes < ws.total)
-      return fail(PA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", ws.total,
+  const Plan pl = make_plan(d, n_rows, num_q_heads, max_blocks_per_seq, chunks, n_chunks,
+                            q_dtype == PA_BF16 && d.kv_dtype == PA_BF16);
+  if (pl.total > 0) {
+    if (workspace == nullptr || workspace_bytes < pl.total)
+      return fail(PA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", pl.total,
                   workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);
     if (!aligned(workspace, 256)) return fail(PA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   }
@@ -224,26 +324,60 @@ pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dt
   p.D = d.head_dim;
   p.q_is_bf16 = q_dtype == PA_BF16;
   p.split_tokens = g_split_tokens;
-  p.max_splits = max_splits;
+  p.max_splits = pl.max_splits;
   p.qk_scale_log2 = static_cast<float>(sm * k_scale * 1.4426950408889634073599246810018921);  // log2(e)
   p.v_scale = d.kv_dtype == PA_FP8_E4M3 ? d.v_scale : 1.0f;
-  if (ws.total > 0) {
+  if (pl.total > 0) {
     unsigned char* base = static_cast<unsigned char*>(workspace);
-    p.ws_count = reinterpret_cast<int32_t*>(base + ws.count_off);
-    p.ws_ml = reinterpret_cast<float*>(base + ws.ml_off);
-    p.ws_o = reinterpret_cast<float*>(base + ws.o_off);
+    if (pl.max_splits > 1) {
+      p.ws_count = reinterpret_cast<int32_t*>(base + pl.d_count);
+      p.ws_ml = reinterpret_cast<float*>(base + pl.d_ml);
+      p.ws_o = reinterpret_cast<float*>(base + pl.d_o);
+    }
+    if (pl.tile_splits > 1) {
+      p.ws_tile_count = reinterpret_cast<int32_t*>(base + pl.t_count);
+      p.ws_tile_ml = reinterpret_cast<float*>(base + pl.t_ml);
+      p.ws_tile_o = reinterpret_cast<float*>(base + pl.t_o);
+    }
   }
   p.status = status_dev;
   p.wait_limit = g_wait_limit;
+  p.debug_stall = g_debug_stall;
   p.n_prefill_ctas = 0;
-  p.n_chunks = 0;  // chunk rows run on the decode path until the tile path takes them
+  p.n_chunks = 0;
+  p.sm_scale_log2 = static_cast<float>(sm * 1.4426950408889634073599246810018921);
+
+  // Chunks long enough for the tensor-core tile path (bf16 q and K/V): their
+  // rows run there; rows of other chunks run as decode rows.
+  if (pl.n_tile > 0) {
+    pa_status st = encode_pool_maps(const_cast<pa_pool*>(pool));
+    if (st != PA_OK) return st;
+    p.kmap = pool->kmap;
+    p.vmap = pool->vmap;
+    p.tile_rows = pl.R;
+    p.tile_splits = pl.tile_splits;
+    p.n_chunks = pl.n_tile;
+    for (int k = 0; k < pl.n_tile; ++k) {
+      p.chunk_begin[k] = chunks[pl.src[k]].row_begin;
+      p.chunk_end[k] = chunks[pl.src[k]].row_begin + chunks[pl.src[k]].n_rows;
+      p.chunk_cta_begin[k] = pl.cta_begin[k];
+      p.chunk_row_begin[k] = pl.row_begin[k];
+      p.chunk_tile_begin[k] = pl.tile_begin[k];
+    }
+    p.chunk_cta_begin[pl.n_tile] = pl.cta_begin[pl.n_tile];
+    p.n_prefill_ctas = pl.cta_begin[pl.n_tile];
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  switch (d.kv_dtype) {
-    case PA_F32: e = pa::launch_decode_f32(p, s); break;
-    case PA_BF16: e = pa::launch_decode_bf16(p, s); break;
-    default: e = pa::launch_decode_e4m3(p, s); break;
+  if (p.n_prefill_ctas > 0) {
+    e = pa::launch_mixed_bf16(p, s);
+  } else {
+    switch (d.kv_dtype) {
+      case PA_F32: e = pa::launch_decode_f32(p, s); break;
+      case PA_BF16: e = pa::launch_decode_bf16(p, s); break;
+      default: e = pa::launch_decode_e4m3(p, s); break;
+    }
   }
   if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "no decode kernel for head_dim %d, group %d", d.head_dim, G);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -260,6 +394,8 @@ pa_status pa_set_split_tokens(int32_t tokens) {
 int32_t pa_get_split_tokens(void) { return g_split_tokens; }
 
 void pa_set_wait_limit(uint32_t polls) { g_wait_limit = polls == 0 ? pa::kDefaultWaitLimit : polls; }
+
+void pa_debug_stall_waits(int32_t enable) { g_debug_stall = enable != 0; }
 
 const char* pa_status_string(pa_status status) {
   switch (status) {

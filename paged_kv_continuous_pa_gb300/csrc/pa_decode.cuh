@@ -101,6 +101,7 @@ struct DecodeGeom {
 // Shared-memory header in front of the stage ring (the ring starts 128-byte aligned).
 struct DecodeSmemHeader {
   uint64_t full[kMaxStages];   // stage landed (bulk-copy bytes)
+  uint64_t stall;              // never completed: the injected-stall test waits here
   int32_t done[kMaxStages];    // warps finished with the stage; the last one refills it
   int32_t bad;                 // a page id was out of range or a wait gave up
   int32_t last;                // this CTA merges the splits of its (row, kv head)
@@ -191,6 +192,49 @@ __device__ __forceinline__ void load_p(const float* src, float (&pv)[G]) {
   }
 }
 
+// N consecutive query elements starting at element i (i a multiple of N; q
+// 16-byte aligned), widened to float, with 4..16-byte loads.
+template <int N>
+__device__ __forceinline__ void load_q_vec(const void* q, bool bf16, size_t i, float* f) {
+  if (bf16) {
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(q) + i;
+    if constexpr (N % 8 == 0) {
+#pragma unroll
+      for (int k = 0; k < N / 8; ++k) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(src) + k);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          f[8 * k + 2 * j] = bf16lo(ws[j]);
+          f[8 * k + 2 * j + 1] = bf16hi(ws[j]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < N / 2; ++k) {
+        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src) + k);
+        f[2 * k] = bf16lo(w);
+        f[2 * k + 1] = bf16hi(w);
+      }
+    }
+  } else {
+    const float* src = reinterpret_cast<const float*>(q) + i;
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+      for (int k = 0; k < N / 4; ++k) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(src) + k);
+        f[4 * k] = v.x;
+        f[4 * k + 1] = v.y;
+        f[4 * k + 2] = v.z;
+        f[4 * k + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < N; ++k) f[k] = __ldg(src + k);
+    }
+  }
+}
+
 __device__ __forceinline__ float load_q(const void* q, bool bf16, size_t i) {
   if (bf16) return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(q)[i]) << 16);
   return reinterpret_cast<const float*>(q)[i];
@@ -261,7 +305,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
   // A row whose sequence or position is out of range: zeros, error recorded once.
   if (seq < 0 || seq >= p.num_seqs || pos < 0 || pos >= p.max_blocks * P) {
     if (split == 0) {
-      for (int i = tid; i < G * D; i += blockDim.x)
+      for (int i = tid; i < G * D; i += Geo::THREADS)
         store_out(p.out, q_bf16, (static_cast<size_t>(row) * p.Hq + h * G) * D + i, 0.0f);
       if (tid == 0) record_error(p.status, ST_OUT_OF_RANGE);
     }
@@ -285,6 +329,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
       mbar_init(&hdr->full[s], 1);
       hdr->done[s] = 0;
     }
+    mbar_init(&hdr->stall, 1);
     hdr->bad = 0;
     hdr->last = 0;
     hdr->issued = 0;
@@ -294,18 +339,18 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
     // the unit's page ids, range-checked before any copy
     const int32_t* bt = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + j0;
     bool bad = false;
-    for (int i = tid; i < npg && i < kMaxUnitPages; i += blockDim.x) {
+    for (int i = tid; i < npg && i < kMaxUnitPages; i += Geo::THREADS) {
       const int pid = __ldg(bt + i);
       bad |= pid < 0 || pid >= p.num_pages;
       hdr->pid[i] = pid;
     }
-    __syncthreads();  // barrier init and zeroed flags visible before the error flag is raised
+    sync_threads_n<Geo::THREADS>();  // barrier init and zeroed flags visible before the error flag is raised
     if (bad) {
       hdr->bad = 1;
       record_error(p.status, ST_OUT_OF_RANGE);
     }
   }
-  __syncthreads();
+  sync_threads_n<Geo::THREADS>();
   const bool unit_bad = hdr->bad != 0;
   const uint64_t policy = l2_policy_evict_first();
   if (tid == 0 && !unit_bad) {
@@ -336,10 +381,9 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int vidx = part + LPT * ((i + tok) % NV);
+        load_q_vec<EPV>(p.q, q_bf16, qrow + static_cast<size_t>(g) * D + vidx * EPV, qr[g][i]);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e)
-          qr[g][i][e] =
-              __fmul_rn(load_q(p.q, q_bf16, qrow + static_cast<size_t>(g) * D + vidx * EPV + e), p.qk_scale_log2);
+        for (int e = 0; e < EPV; ++e) qr[g][i][e] = __fmul_rn(qr[g][i][e], p.qk_scale_log2);
       }
   }
   float* pbuf = &hdr->p[warp][0][0];
@@ -348,7 +392,9 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
 
   for (int n = 0; n < nstage && !unit_bad; ++n) {
     const int s = n % nst;
-    const bool landed = __all_sync(0xffffffffu, mbar_wait(&hdr->full[s], (n / nst) & 1, p.wait_limit));
+    bool got = mbar_wait(&hdr->full[s], (n / nst) & 1, p.wait_limit);
+    if (p.debug_stall) got = got && mbar_wait(&hdr->stall, 0, p.wait_limit);  // runs out by construction
+    const bool landed = __all_sync(0xffffffffu, got);
     if (!landed) {
       if (lane == 0) {
         record_error(p.status, ST_TIMEOUT);
@@ -464,13 +510,13 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
       for (int off = PLT; off < 32; off <<= 1) acc[g][e] = __fadd_rn(acc[g][e], __shfl_xor_sync(0xffffffffu, acc[g][e], off));
   }
 
-  __syncthreads();
+  sync_threads_n<Geo::THREADS>();
   if (tid == 0) {
     // every issued copy must land before the ring is reused (only matters after a timeout)
     const int issued = hdr->issued;
     for (int n = max(0, issued - nst); n < issued; ++n) mbar_wait(&hdr->full[n % nst], (n / nst) & 1, kDrainWaitLimit);
   }
-  __syncthreads();
+  sync_threads_n<Geo::THREADS>();
 
   // ---- merge the 4 warps' states, warp 0 first
   float* red_acc = reinterpret_cast<float*>(ring);  // [NW][G][D]
@@ -486,11 +532,11 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
       red_ml[(warp * G + g) * 2 + 1] = l_run[g];
     }
   }
-  __syncthreads();
+  sync_threads_n<Geo::THREADS>();
   const bool bad = hdr->bad != 0;
   const size_t out_row = static_cast<size_t>(row) * p.Hq + static_cast<size_t>(h) * G;
   if (nsplit == 1) {
-    for (int i = tid; i < G * D; i += blockDim.x) {
+    for (int i = tid; i < G * D; i += Geo::THREADS) {
       const int g = i / D, d = i % D;
       float M = -INFINITY;
 #pragma unroll
@@ -510,7 +556,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
   }
 
   // ---- split row: publish this split's partial triple, the last split merges
-  for (int i = tid; i < G * D; i += blockDim.x) {
+  for (int i = tid; i < G * D; i += Geo::THREADS) {
     const int g = i / D, d = i % D;
     float M = -INFINITY;
 #pragma unroll
@@ -535,26 +581,62 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
     }
   }
   __threadfence();
-  __syncthreads();
+  sync_threads_n<Geo::THREADS>();
   int32_t* counter = p.ws_count + static_cast<size_t>(row) * p.Hkv + h;
   if (tid == 0) hdr->last = (atomicAdd(counter, 1) == nsplit - 1) ? 1 : 0;
-  __syncthreads();
+  sync_threads_n<Geo::THREADS>();
   if (!hdr->last) return;
   __threadfence();
-  for (int i = tid; i < G * D; i += blockDim.x) {
-    const int g = i / D, d = i % D;
-    const size_t slot0 = (out_row + g) * p.max_splits;
-    float M = -INFINITY;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(p.ws_ml + (slot0 + sp) * 2));
-    float lsum = 0.0f, osum = 0.0f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const float f = ex2(__fsub_rn(__ldcg(p.ws_ml + (slot0 + sp) * 2), M));
-      lsum = fmaf(f, __ldcg(p.ws_ml + (slot0 + sp) * 2 + 1), lsum);
-      osum = fmaf(f, __ldcg(p.ws_o + (slot0 + sp) * D + d), osum);
+  // Merge the splits in ascending order.  The (max, sum) pairs go through
+  // shared memory first, so the value loads below are independent and coalesced.
+  const size_t slot_base = out_row * p.max_splits;  // slot of (head 0 of the group, split 0)
+  float* fbuf = red_acc + NW * G * D + NW * G * 2;   // [G][nsplit] weights, then [G] sums
+  const int ring_floats = p.n_stages * Geo::STAGE_BYTES / 4 - (NW * G * D + NW * G * 2);
+  if (G * (nsplit + 1) <= ring_floats) {
+    for (int i = tid; i < G * nsplit; i += Geo::THREADS) {
+      const int g = i / nsplit, sp = i % nsplit;
+      fbuf[i] = __ldcg(p.ws_ml + (slot_base + static_cast<size_t>(g) * p.max_splits + sp) * 2);
     }
-    float o = __fdiv_rn(osum, lsum);
-    if (KVT == KV_E4M3) o = __fmul_rn(o, p.v_scale);
-    store_out(p.out, q_bf16, out_row * D + i, o);
+    sync_threads_n<Geo::THREADS>();
+    if (tid < G) {
+      const int g = tid;
+      float M = -INFINITY;
+      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, fbuf[g * nsplit + sp]);
+      float lsum = 0.0f;
+      for (int sp = 0; sp < nsplit; ++sp) {
+        const float f = ex2(__fsub_rn(fbuf[g * nsplit + sp], M));
+        fbuf[g * nsplit + sp] = f;
+        lsum = fmaf(f, __ldcg(p.ws_ml + (slot_base + static_cast<size_t>(g) * p.max_splits + sp) * 2 + 1), lsum);
+      }
+      fbuf[G * nsplit + g] = lsum;
+    }
+    sync_threads_n<Geo::THREADS>();
+    for (int i = tid; i < G * D; i += Geo::THREADS) {
+      const int g = i / D, d = i % D;
+      const float* o = p.ws_o + (slot_base + static_cast<size_t>(g) * p.max_splits) * D + d;
+      float osum = 0.0f;
+#pragma unroll 4
+      for (int sp = 0; sp < nsplit; ++sp) osum = fmaf(fbuf[g * nsplit + sp], __ldcg(o + static_cast<size_t>(sp) * D), osum);
+      float out = __fdiv_rn(osum, fbuf[G * nsplit + g]);
+      if (KVT == KV_E4M3) out = __fmul_rn(out, p.v_scale);
+      store_out(p.out, q_bf16, out_row * D + i, out);
+    }
+  } else {
+    for (int i = tid; i < G * D; i += Geo::THREADS) {
+      const int g = i / D, d = i % D;
+      const size_t slot0 = (out_row + g) * p.max_splits;
+      float M = -INFINITY;
+      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(p.ws_ml + (slot0 + sp) * 2));
+      float lsum = 0.0f, osum = 0.0f;
+      for (int sp = 0; sp < nsplit; ++sp) {
+        const float f = ex2(__fsub_rn(__ldcg(p.ws_ml + (slot0 + sp) * 2), M));
+        lsum = fmaf(f, __ldcg(p.ws_ml + (slot0 + sp) * 2 + 1), lsum);
+        osum = fmaf(f, __ldcg(p.ws_o + (slot0 + sp) * D + d), osum);
+      }
+      float out = __fdiv_rn(osum, lsum);
+      if (KVT == KV_E4M3) out = __fmul_rn(out, p.v_scale);
+      store_out(p.out, q_bf16, out_row * D + i, out);
+    }
   }
   if (tid == 0) *counter = 0;  // leave the workspace zero-filled for the next call
 }
@@ -566,7 +648,7 @@ __global__ void __launch_bounds__(DecodeGeom<D, G, KVT>::THREADS, DecodeGeom<D, 
 }
 
 template <int D, int G, int KVT>
-size_t decode_smem_for(int P, int n_stages) {
+__host__ __device__ constexpr size_t decode_smem_for(int P, int n_stages) {
   using Geo = DecodeGeom<D, G, KVT>;
   (void)P;
   const size_t ring = static_cast<size_t>(n_stages) * 2 * kStageTokens * Geo::RB;

@@ -92,6 +92,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
+// Barrier over the first NT threads of the CTA (named barrier 1), for code
+// that runs in a CTA whose remaining warps have other work or have exited.
+template <int NT>
+__device__ __forceinline__ void sync_threads_n() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+
 // Order this thread's generic-proxy shared-memory accesses before its later
 // async-proxy (bulk-copy) operations on shared memory.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

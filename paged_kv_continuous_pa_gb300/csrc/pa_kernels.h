@@ -2,6 +2,7 @@
 // kernels.  Internal: not part of the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -72,11 +73,23 @@ struct AttnParams {
   int32_t* ws_count;     // [n_rows][Hkv] finished-split counters, zero between calls
   int32_t* status;
   uint32_t wait_limit;
+  int32_t debug_stall;   // 1: every CTA also waits on a barrier nothing completes (failure-path test)
   int32_t n_stages;      // decode pipeline depth (set per instantiation at launch)
   int32_t n_prefill_ctas;  // CTAs [0, n_prefill_ctas) run prefill tiles, the rest decode units
-  int32_t n_chunks;
-  int32_t chunk_begin[kMaxChunks];
+  int32_t n_chunks;                       // chunks on the tensor-core tile path
+  int32_t chunk_begin[kMaxChunks];        // their rows [chunk_begin, chunk_end)
   int32_t chunk_end[kMaxChunks];
+  int32_t chunk_cta_begin[kMaxChunks + 1];  // prefix sums of tile CTAs per chunk
+  int32_t chunk_row_begin[kMaxChunks];    // prefix sums of chunk rows (tile partial slots)
+  int32_t chunk_tile_begin[kMaxChunks];   // prefix sums of tiles (tile counters)
+  int32_t tile_rows;                      // positions per 128-row tile: 128 / G
+  int32_t tile_splits;                    // key-range splits per tile (CTAs per tile)
+  float* ws_tile_o;                       // [chunk rows][Hq][tile_splits][D] partial accumulators
+  float* ws_tile_ml;                      // [chunk rows][Hq][tile_splits][2] partial (max, sum)
+  int32_t* ws_tile_count;                 // [tiles] finished-split counters, zero between calls
+  float sm_scale_log2;                    // softmax scale * log2(e) for the tile path
+  CUtensorMap kmap;                       // K pool as [num_pages * Hkv * P][D] bf16, box 64 x P, 128B swizzle
+  CUtensorMap vmap;                       // V pool, same geometry
 };
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
@@ -92,6 +105,17 @@ void set_last_error(const char* fmt, ...);
 cudaError_t launch_decode_f32(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_decode_e4m3(const AttnParams& p, cudaStream_t stream);
+
+// One launch whose first p.n_prefill_ctas CTAs run tensor-core prefill tiles
+// (bf16 q and K/V) and whose remaining CTAs run decode units.
+cudaError_t launch_mixed_bf16(const AttnParams& p, cudaStream_t stream);
+
+constexpr int kMinTileRows = 16;     // shorter chunks run on the decode path
+constexpr int kTileRowsTotal = 128;  // (position, head) rows of one tensor-core tile
+#ifndef PA_TILE_SPLIT_KEYS
+#define PA_TILE_SPLIT_KEYS 4096
+#endif
+constexpr int kTileSplitKeys = PA_TILE_SPLIT_KEYS;  // keys per CTA of a tile (a multiple of 64); longer tiles split
 
 
 }  // namespace pa

@@ -65,7 +65,7 @@ extern "C" pa_status pa_attention_noalloc(const pa_pool* pool, int32_t n_rows, c
                                           const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
                                           const pa_chunk* chunks, int32_t n_chunks, float softmax_scale, void* out,
                                           int32_t* status_dev, void* stream) {
-  const size_t need = pa_attention_workspace_bytes(pool, n_rows, num_q_heads, max_blocks_per_seq);
+  const size_t need = pa_attention_workspace_bytes(pool, n_rows, num_q_heads, max_blocks_per_seq, chunks, n_chunks);
   if (need > kNoallocScratchBytes) {
     pa::set_last_error(
         "pa_attention_noalloc: this call needs %zu bytes of split-KV scratch but the static scratch holds %zu; "

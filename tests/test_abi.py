@@ -88,12 +88,16 @@ def test_host_side_errors_launch_nothing(lib):
         assert att(chunks=None, nc=1) == pa.PA_ERR_INVALID_ARG
         assert att(nc=17) == pa.PA_ERR_INVALID_ARG
         # long tables need a workspace for split partials
-        need = lib.pa_attention_workspace_bytes(h, 4, 8, 200)
+        need = lib.pa_attention_workspace_bytes(h, 4, 8, 200, None, 0)
         assert need > 0 and need % 256 == 0
         assert att(mb=200) == pa.PA_ERR_INVALID_ARG
         assert att(mb=200, ws=vp(0x200000), wsb=need - 1) == pa.PA_ERR_INVALID_ARG
         assert att(mb=200, ws=vp(0x200010), wsb=need) == pa.PA_ERR_INVALID_ARG  # not 256-aligned
-        assert lib.pa_attention_workspace_bytes(h, 4, 8, 4) == 0  # 128 tokens: never split
+        assert lib.pa_attention_workspace_bytes(h, 4, 8, 4, None, 0) == 0  # 128 tokens: never split
+        one = (pa.Chunk * 1)(pa.Chunk(0, 4))
+        assert lib.pa_attention_workspace_bytes(h, 4, 8, 4, one, 1) == 0  # chunk below the tile threshold
+        big = (pa.Chunk * 1)(pa.Chunk(0, 64))
+        assert lib.pa_attention_workspace_bytes(h, 64, 8, 40, big, 1) > 0  # 1280 keys: tile key ranges split
     finally:
         lib.pa_pool_destroy(h)
 

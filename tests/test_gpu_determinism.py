@@ -18,7 +18,7 @@ def attend_rows(st, rows, chunks=()):
     q = st.q[rows].contiguous()
     out = torch.empty_like(q)
     n = q.shape[0]
-    wsb = pa.workspace_bytes(st.pool, n, st.wl.Hq, st.wl.max_blocks)
+    wsb = pa.workspace_bytes(st.pool, n, st.wl.Hq, st.wl.max_blocks, chunks)
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda") if wsb else None
     pa.attention(st.pool, q, st.seq_ids[rows].contiguous(), st.positions[rows].contiguous(), st.block_tables, out,
                  chunks=chunks, workspace=ws, status=st.status)

@@ -60,11 +60,16 @@ def test_bad_page_id_reports(step):
 
 
 def test_wait_limit_runs_out_cleanly_and_context_survives(step):
+    """Every CTA waits on a barrier nothing completes (the library's injected
+    stall): the bounded wait runs out, the call reports PA_ERR_TIMEOUT, and the
+    next normal call on the same context gives the same bits as before."""
     good = step.out.clone()
-    pa.set_wait_limit(1)
+    pa.set_wait_limit(1000)
+    pa.debug_stall_waits(True)
     try:
         code, _ = _run(step)
     finally:
+        pa.debug_stall_waits(False)
         pa.set_wait_limit(0)
     assert code == pa.PA_ERR_TIMEOUT
     code, out = _run(step)

@@ -1,0 +1,114 @@
+"""The tensor-core prefill-chunk tile path (tcgen05) against the oracle:
+chunk lengths that leave ragged tiles, chunks starting at position 0, keys
+past the chunk's last row on poisoned slots, several chunks and decode rows in
+one launch, every group size, both head dims and all page sizes."""
+import numpy as np
+import pytest
+import torch
+
+import pa_setup
+import paged_kv_continuous_pa_gb300 as pa
+import workloads as W
+from ref import assert_close, oracle_out, oracle_pools
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_check(wl, what):
+    st = pa_setup.upload(wl)
+    st.append_step()
+    st.attend()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0, f"device status {int(st.status.item())}"
+    kp, vp = oracle_pools(wl)
+    ref = oracle_out(wl, kp, vp)
+    got = W.bf16_bits_to_f32(pa_setup.to_numpy(st.out)).astype(np.float64)
+    return assert_close(got, ref, wl, what)
+
+
+@pytest.mark.parametrize("chunk", [(0, 16, 16), (0, 130, 150), (37, 64, 200), (100, 300, 420), (64, 257, 321)])
+def test_single_chunk_shapes(chunk):
+    run_and_check(W.chunked_step(11, [chunk]), f"chunk {chunk}")
+
+
+@pytest.mark.parametrize("G", [1, 3, 4, 5, 8])
+def test_group_sizes(G):
+    run_and_check(W.chunked_step(20 + G, [(50, 140, 200)], decode_ctx=[70, 500], Hq=2 * G, Hkv=2), f"G{G}")
+
+
+@pytest.mark.parametrize("D,P", [(64, 16), (64, 64), (128, 16), (128, 64)])
+def test_head_dims_and_pages(D, P):
+    run_and_check(W.chunked_step(30 + D + P, [(33, 97, 180)], decode_ctx=[5, 300], Hq=8, Hkv=2, D=D, P=P),
+                  f"D{D} P{P}")
+
+
+def test_long_tile_key_ranges_split_and_merge():
+    """A chunk far into its sequence: each tile's keys span several key ranges
+    that separate CTAs process and the last one merges in ascending order."""
+    wl = W.chunked_step(45, [(9000, 200, 9300)], decode_ctx=[50, 7000], Hq=8, Hkv=2)
+    run_and_check(wl, "chunk at 9000")
+
+
+def test_several_chunks_with_decode_rows():
+    wl = W.chunked_step(41, [(0, 40, 40), (200, 77, 300), (513, 128, 700)], decode_ctx=[1, 64, 999, 2000])
+    run_and_check(wl, "three chunks + decode rows")
+
+
+def test_chunk_rows_bit_identical_across_calls_and_batches():
+    wl = W.chunked_step(51, [(300, 200, 600)], decode_ctx=[10, 400, 900])
+    st = pa_setup.upload(wl)
+    st.append_step()
+    st.attend()
+    torch.cuda.synchronize()
+    first = st.out.view(torch.int16).clone()
+    for _ in range(5):
+        st.attend()
+        torch.cuda.synchronize()
+        assert torch.equal(st.out.view(torch.int16), first)
+    # the chunk alone (no decode rows in the launch) gives the same chunk bits
+    b, n = wl.chunks[0]
+    sl = slice(b, b + n)
+    out = torch.empty_like(st.q[sl])
+    wsb = pa.workspace_bytes(st.pool, n, wl.Hq, wl.max_blocks, [(0, n)])
+    ws = torch.zeros(max(wsb, 1), dtype=torch.uint8, device="cuda")
+    pa.attention(st.pool, st.q[sl].contiguous(), st.seq_ids[sl].contiguous(), st.positions[sl].contiguous(),
+                 st.block_tables, out, chunks=[(0, n)], workspace=ws, status=st.status)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), first[sl])
+
+
+def test_short_chunk_and_f32_queries_use_the_decode_path():
+    # 15 rows is below the tile threshold; f32 q cannot use the bf16 tensor cores
+    run_and_check(W.chunked_step(61, [(20, 15, 40)], decode_ctx=[30]), "short chunk")
+    wl = W.chunked_step(62, [(20, 90, 200)], decode_ctx=[30], q_dtype=W.F32, kv_dtype=W.F32)
+    st = pa_setup.upload(wl)
+    st.append_step()
+    st.attend()
+    torch.cuda.synchronize()
+    kp, vp = oracle_pools(wl)
+    assert_close(pa_setup.to_numpy(st.out).astype(np.float64), oracle_out(wl, kp, vp), wl, "f32 chunk")
+
+
+def test_tile_path_timeout_reports_and_recovers():
+    wl = W.chunked_step(71, [(500, 256, 800)], decode_ctx=[100, 2000])
+    st = pa_setup.upload(wl)
+    st.append_step()
+    st.attend()
+    torch.cuda.synchronize()
+    good = st.out.view(torch.int16).clone()
+    pa.set_wait_limit(1000)
+    pa.debug_stall_waits(True)
+    try:
+        st.status.zero_()
+        st.attend()
+        torch.cuda.synchronize()
+        code = int(st.status.item())
+    finally:
+        pa.debug_stall_waits(False)
+        pa.set_wait_limit(0)
+    assert code == pa.PA_ERR_TIMEOUT
+    st.status.zero_()
+    st.attend()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    assert torch.equal(st.out.view(torch.int16), good)

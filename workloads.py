@@ -372,6 +372,47 @@ def shared_prefix(seed: int = 4, n_seqs: int = 768, share_frac: float = 0.7, pre
                                 f"generated, {n_share} seqs share a {prefix}-token prefix, P32")
 
 
+def chunked_step(seed: int, chunks, decode_ctx=(), Hq: int = 16, Hkv: int = 8, D: int = 128, P: int = 32,
+                 q_dtype: int = BF16, kv_dtype: int = BF16, spare_pages: int = 8) -> Workload:
+    """Decode rows (one per context in decode_ctx) followed by prefill chunks;
+    chunks = [(chunk_start, chunk_len, reserved_tokens)], one sequence each, whose
+    tokens 0..chunk_start-1 are history.  Pages for reserved_tokens are taken
+    up front, so the chunk's last page may hold slots past its last row."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    decode_ctx = [int(x) for x in decode_ctx]
+    n_dec = len(decode_ctx)
+    reserve = [max(L, 1) for L in decode_ctx] + [int(r) for _, _, r in chunks]
+    pages = [(r + P - 1) // P for r in reserve]
+    max_blocks = max(pages)
+    num_pages = sum(pages) + spare_pages
+    bt = _assign_pages(rng, pages, num_pages, max_blocks)
+    hist_counts = [L - 1 for L in decode_ctx] + [int(c0) for c0, _, _ in chunks]
+    ns = n_dec + len(chunks)
+    hist_seq = np.repeat(np.arange(ns, dtype=np.int32), hist_counts)
+    hist_pos = np.concatenate([np.arange(c, dtype=np.int32) for c in hist_counts]) if ns else np.zeros(0, np.int32)
+    in_dtype = kv_dtype if kv_dtype != E4M3 else BF16
+    hist_k, hist_v = _draw_rows(seed * 1000 + 1, hist_counts, Hkv, D, in_dtype)
+    seq_ids = [np.arange(n_dec, dtype=np.int32)]
+    positions = [np.array(decode_ctx, dtype=np.int32) - 1]
+    spans = []
+    row = n_dec
+    for i, (c0, cl, _) in enumerate(chunks):
+        seq_ids.append(np.full(cl, n_dec + i, dtype=np.int32))
+        positions.append(np.arange(c0, c0 + cl, dtype=np.int32))
+        spans.append((row, cl))
+        row += cl
+    seq_ids = np.concatenate(seq_ids)
+    positions = np.concatenate(positions)
+    n = len(seq_ids)
+    q = _cast(rng.standard_normal((n, Hq, D), dtype=np.float32), q_dtype)
+    k_new = _cast(rng.standard_normal((n, Hkv, D), dtype=np.float32), in_dtype)
+    v_new = _cast(rng.standard_normal((n, Hkv, D), dtype=np.float32), in_dtype)
+    return Workload(name="chunked", Hq=Hq, Hkv=Hkv, D=D, P=P, kv_dtype=kv_dtype, in_dtype=in_dtype, q_dtype=q_dtype,
+                    num_pages=num_pages, block_tables=bt, hist_seq=hist_seq, hist_pos=hist_pos, hist_k=hist_k,
+                    hist_v=hist_v, seq_ids=seq_ids, positions=positions, q=q, k_new=k_new, v_new=v_new,
+                    chunks=spans, description=f"chunked step: {n_dec} decode rows + chunks {list(chunks)}")
+
+
 CONFIGS = {
     "tiny_decode": tiny_decode,
     "batched_decode": batched_decode,
