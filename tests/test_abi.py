@@ -97,7 +97,8 @@ def test_host_side_errors_launch_nothing(lib):
         one = (pa.Chunk * 1)(pa.Chunk(0, 4))
         assert lib.pa_attention_workspace_bytes(h, 4, 8, 4, one, 1) == 0  # chunk below the tile threshold
         big = (pa.Chunk * 1)(pa.Chunk(0, 64))
-        assert lib.pa_attention_workspace_bytes(h, 64, 8, 40, big, 1) > 0  # 1280 keys: tile key ranges split
+        # 6400 keys: tile key ranges split (4096 keys per range), on top of the decode splits
+        assert lib.pa_attention_workspace_bytes(h, 64, 8, 200, big, 1) > lib.pa_attention_workspace_bytes(h, 64, 8, 200, None, 0)
     finally:
         lib.pa_pool_destroy(h)
 
