@@ -23,8 +23,9 @@
 // H100 page describes cannot occur).
 // Work split inside a stage: warp w owns tokens 8w .. 8w+7.  For Q.K, LPT
 // lanes share one token and each dots its D / LPT elements with the matching
-// slice of the G query vectors held in registers; a fixed xor-butterfly over
-// the LPT lanes completes the dot product.  One online-softmax update covers
+// slice of the G query vectors held in registers (packed two-wide FMAs, even
+// and odd elements summed at the end); a fixed xor-butterfly over the LPT
+// lanes completes the dot product.  One online-softmax update covers
 // the warp's 8 tokens.  For P.V, PLT lanes share one token and each owns PE
 // consecutive output elements.
 //
@@ -420,10 +421,12 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
           load_widen<KVT, Geo::VEC>(krow + vidx * Geo::VEC, kf);
 #pragma unroll
           for (int g = 0; g < G; ++g) {
-            float a = __fmul_rn(qr[g][i][0], kf[0]);
+            // even and odd elements in the two halves of a packed FMA, then added
+            float2 a = __fmul2_rn(make_float2(qr[g][i][0], qr[g][i][1]), make_float2(kf[0], kf[1]));
 #pragma unroll
-            for (int e = 1; e < EPV; ++e) a = fmaf(qr[g][i][e], kf[e], a);
-            partial[g][i] = a;
+            for (int e = 2; e < EPV; e += 2)
+              a = __ffma2_rn(make_float2(qr[g][i][e], qr[g][i][e + 1]), make_float2(kf[e], kf[e + 1]), a);
+            partial[g][i] = __fadd_rn(a.x, a.y);
           }
         }
 #pragma unroll
@@ -451,7 +454,11 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
           m_ref[g] = mx;
           l_run[g] = __fmul_rn(l_run[g], alpha);
 #pragma unroll
-          for (int e = 0; e < PE; ++e) acc[g][e] = __fmul_rn(acc[g][e], alpha);
+          for (int e = 0; e < PE; e += 2) {
+            const float2 a = __fmul2_rn(make_float2(acc[g][e], acc[g][e + 1]), make_float2(alpha, alpha));
+            acc[g][e] = a.x;
+            acc[g][e + 1] = a.y;
+          }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {  // scores become weights in place
@@ -479,7 +486,12 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
 #pragma unroll
           for (int g = 0; g < G; ++g)
 #pragma unroll
-            for (int e = 0; e < PE; ++e) acc[g][e] = fmaf(pv[g], vf[e], acc[g][e]);
+            for (int e = 0; e < PE; e += 2) {
+              const float2 a = __ffma2_rn(make_float2(pv[g], pv[g]), make_float2(vf[e], vf[e + 1]),
+                                          make_float2(acc[g][e], acc[g][e + 1]));
+              acc[g][e] = a.x;
+              acc[g][e + 1] = a.y;
+            }
         }
       }
     }
