@@ -181,17 +181,16 @@ pa_status pa_attention_noalloc(const pa_pool *pool, int32_t n_rows, const void *
 pa_status pa_set_split_tokens(int32_t tokens);
 int32_t pa_get_split_tokens(void);
 
-/* Upper bound on the polls of one device-side wait before it gives up with
- * PA_ERR_TIMEOUT (0 restores the default of about a second).  A debugging
- * knob: with 1, waits give up almost at once, which exercises the error path
- * without any real hang. */
-void pa_set_wait_limit(uint32_t polls);
+/* Longest time, in microseconds, one device-side wait (for a copy or an MMA
+ * to complete) may take before it gives up with PA_ERR_TIMEOUT; 0 restores
+ * the default of one second.  A debugging knob for failure-path tests. */
+void pa_set_wait_limit(uint32_t microseconds);
 
 /* Failure-path testing without a GPU fault: with enable != 0, every attention
  * CTA additionally waits on a barrier that nothing ever completes, so that
  * wait runs out after the current wait limit; the call then reports
  * PA_ERR_TIMEOUT in *status_dev, its outputs are unspecified, and the kernel
- * still returns normally.  Set a small wait limit first (e.g. 1000 polls).
+ * still returns normally.  Set a small wait limit first (e.g. 1000 us).
  * Off by default; affects calls made while it is on. */
 void pa_debug_stall_waits(int32_t enable);
 

@@ -231,8 +231,8 @@ def get_split_tokens() -> int:
     return int(load().pa_get_split_tokens())
 
 
-def set_wait_limit(polls: int):
-    load().pa_set_wait_limit(int(polls))
+def set_wait_limit(microseconds: int):
+    load().pa_set_wait_limit(int(microseconds))
 
 
 def kernel_launches() -> int:

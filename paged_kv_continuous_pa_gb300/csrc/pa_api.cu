@@ -393,7 +393,7 @@ pa_status pa_set_split_tokens(int32_t tokens) {
 
 int32_t pa_get_split_tokens(void) { return g_split_tokens; }
 
-void pa_set_wait_limit(uint32_t polls) { g_wait_limit = polls == 0 ? pa::kDefaultWaitLimit : polls; }
+void pa_set_wait_limit(uint32_t microseconds) { g_wait_limit = microseconds == 0 ? pa::kDefaultWaitLimit : microseconds; }
 
 void pa_debug_stall_waits(int32_t enable) { g_debug_stall = enable != 0; }
 

@@ -255,29 +255,138 @@ __device__ __forceinline__ bool row_in_chunk(const AttnParams& p, int row) {
 }
 
 // Copy the valid token slots of stage n (tokens t_begin + 32n .. +32, clipped
-// to t_end) into its ring slot: one bulk copy of K and one of V per page piece.
+// to t_end) into ring slot s: one bulk copy of K and one of V per page piece.
+// P is a power of two (lg_p = log2 P).
 template <int RB>
 __device__ __forceinline__ void issue_stage(const AttnParams& p, DecodeSmemHeader* hdr, unsigned char* ring, int n,
-                                            int nst, int t_begin, int t_end, int j0, int h, uint64_t policy) {
-  const int s = n % nst;
+                                            int s, int t_begin, int t_end, int j0, int h, int lg_p, uint64_t policy) {
   const int a = t_begin + n * kStageTokens;
   const int b = min(t_end, a + kStageTokens);
   unsigned char* ks = ring + static_cast<size_t>(s) * 2 * kStageTokens * RB;
   unsigned char* vs = ks + kStageTokens * RB;
-  const size_t head_bytes = static_cast<size_t>(p.P) * RB;
+  const size_t head_bytes = static_cast<size_t>(RB) << lg_p;
   const size_t page_bytes = head_bytes * p.Hkv;
   const unsigned char* kb = reinterpret_cast<const unsigned char*>(p.k_pool) + h * head_bytes;
   const unsigned char* vb = reinterpret_cast<const unsigned char*>(p.v_pool) + h * head_bytes;
   mbar_arrive_expect_tx(&hdr->full[s], static_cast<uint32_t>(2 * (b - a) * RB));
   for (int t = a; t < b;) {
-    const int page = hdr->pid[t / p.P - j0];
-    const int slot = t % p.P;
-    const int cnt = min(p.P - slot, b - t);
+    const int page = hdr->pid[(t >> lg_p) - j0];
+    const int slot = t & ((1 << lg_p) - 1);
+    const int cnt = min((1 << lg_p) - slot, b - t);
     const size_t src = static_cast<size_t>(page) * page_bytes + static_cast<size_t>(slot) * RB;
     const size_t dst = static_cast<size_t>(t - a) * RB;
     bulk_g2s(ks + dst, kb + src, static_cast<uint32_t>(cnt * RB), &hdr->full[s], policy);
     bulk_g2s(vs + dst, vb + src, static_cast<uint32_t>(cnt * RB), &hdr->full[s], policy);
     t += cnt;
+  }
+}
+
+// A warp's running softmax state and its query slice (all in registers).
+template <int G, int NV, int EPV, int PE>
+struct DecodeState {
+  float qr[G][NV][EPV];  // query slice, pre-scaled into the log2 domain
+  float m_ref[G];        // reference maximum (log2 domain)
+  float l_run[G];        // this lane's share of the sum of weights
+  float acc[G][PE];      // this lane's share of sum(weight * V)
+};
+
+// One warp's work on one 32-token stage: scores of its WT tokens, one
+// online-softmax update, weights to the warp's exchange buffer, P.V.  FULL:
+// every token of the warp is valid (all stages but the last), no masking.
+template <int D, int G, int KVT, bool FULL>
+__device__ __forceinline__ void decode_stage(DecodeState<G, DecodeGeom<D, G, KVT>::NV, DecodeGeom<D, G, KVT>::EPV,
+                                                         DecodeGeom<D, G, KVT>::PE>& st,
+                                             const unsigned char* krows, const unsigned char* vrows, float* pbuf,
+                                             int n_valid, int tok, int part, int pv_tok, int pv_off) {
+  using Geo = DecodeGeom<D, G, KVT>;
+  constexpr int LPT = Geo::LPT, TPS = Geo::TPS, U = Geo::U, NV = Geo::NV, EPV = Geo::EPV;
+  constexpr int PE = Geo::PE, PLT = Geo::PLT, TPV = Geo::TPV, NPV = Geo::NPV, RB = Geo::RB;
+  (void)PLT;
+  // ---- scores of the warp's tokens (log2 domain), U sub-steps of TPS tokens
+  float sc[U][G];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const unsigned char* krow = krows + static_cast<size_t>(u * TPS + tok) * RB;
+    float partial[G][NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int vidx = part + LPT * ((i + tok) % NV);
+      float kf[EPV];
+      load_widen<KVT, Geo::VEC>(krow + vidx * Geo::VEC, kf);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        // even and odd elements in the two halves of a packed FMA, then added
+        float2 a = __fmul2_rn(make_float2(st.qr[g][i][0], st.qr[g][i][1]), make_float2(kf[0], kf[1]));
+#pragma unroll
+        for (int e = 2; e < EPV; e += 2)
+          a = __ffma2_rn(make_float2(st.qr[g][i][e], st.qr[g][i][e + 1]), make_float2(kf[e], kf[e + 1]), a);
+        partial[g][i] = __fadd_rn(a.x, a.y);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float a = partial[g][0];
+#pragma unroll
+      for (int i = 1; i < NV; ++i) a = __fadd_rn(a, partial[g][i]);
+#pragma unroll
+      for (int off = 1; off < LPT; off <<= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, off));
+      sc[u][g] = (FULL || u * TPS + tok < n_valid) ? a : -INFINITY;
+    }
+  }
+  // ---- online softmax: one reference-max update per stage.  The reference
+  // only moves when the new maximum exceeds it by more than kRescaleSlack
+  // (log2 units), so weights stay <= 2^kRescaleSlack and rescaling is rare.
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float mx = sc[0][g];
+#pragma unroll
+    for (int u = 1; u < U; ++u) mx = fmaxf(mx, sc[u][g]);
+#pragma unroll
+    for (int off = LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (mx > __fadd_rn(st.m_ref[g], kRescaleSlack)) {
+      const float alpha = ex2(__fsub_rn(st.m_ref[g], mx));
+      st.m_ref[g] = mx;
+      st.l_run[g] = __fmul_rn(st.l_run[g], alpha);
+#pragma unroll
+      for (int e = 0; e < PE; e += 2) {
+        const float2 a = __fmul2_rn(make_float2(st.acc[g][e], st.acc[g][e + 1]), make_float2(alpha, alpha));
+        st.acc[g][e] = a.x;
+        st.acc[g][e + 1] = a.y;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {  // scores become weights in place
+      sc[u][g] = (FULL || u * TPS + tok < n_valid) ? ex2(__fsub_rn(sc[u][g], st.m_ref[g])) : 0.0f;
+      st.l_run[g] = __fadd_rn(st.l_run[g], sc[u][g]);
+    }
+  }
+  __syncwarp();
+  if (part == 0) {
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int g = 0; g < G; ++g) pbuf[(u * TPS + tok) * 8 + g] = sc[u][g];
+  }
+  __syncwarp();
+  // ---- acc += p . V over the warp's valid tokens, TPV tokens per iteration
+#pragma unroll
+  for (int it = 0; it < NPV; ++it) {
+    const int t = it * TPV + pv_tok;
+    if (FULL || t < n_valid) {
+      float vf[PE];
+      load_widen<KVT, Geo::VB>(vrows + static_cast<size_t>(t) * RB + pv_off, vf);
+      float pv[G];
+      load_p<G>(pbuf + t * 8, pv);
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < PE; e += 2) {
+          const float2 a = __ffma2_rn(make_float2(pv[g], pv[g]), make_float2(vf[e], vf[e + 1]),
+                                      make_float2(st.acc[g][e], st.acc[g][e + 1]));
+          st.acc[g][e] = a.x;
+          st.acc[g][e + 1] = a.y;
+        }
+    }
   }
 }
 
@@ -321,12 +430,13 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
   const int j0 = t_begin / P;
   const int npg = (t_end + P - 1) / P - j0;
   const int nstage = (t_end - t_begin + ST - 1) / ST;
-  const int nst = p.n_stages;
+  constexpr int NST = Geo::STAGES;
+  const int lg_p = 31 - __clz(P);
 
   DecodeSmemHeader* hdr = reinterpret_cast<DecodeSmemHeader*>(smem);
   unsigned char* ring = smem + decode_header_bytes();
   if (tid == 0) {
-    for (int s = 0; s < nst; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&hdr->full[s], 1);
       hdr->done[s] = 0;
     }
@@ -355,26 +465,25 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
   const bool unit_bad = hdr->bad != 0;
   const uint64_t policy = l2_policy_evict_first();
   if (tid == 0 && !unit_bad) {
-    const int first = min(nst, nstage);
-    for (int n = 0; n < first; ++n) issue_stage<RB>(p, hdr, ring, n, nst, t_begin, t_end, j0, h, policy);
+    const int first = min(NST, nstage);
+    for (int n = 0; n < first; ++n) issue_stage<RB>(p, hdr, ring, n, n, t_begin, t_end, j0, h, lg_p, policy);
     hdr->issued = first;
   }
 
   // ---- per-warp state
-  float m_ref[G], l_run[G], acc[G][PE];
+  DecodeState<G, NV, EPV, PE> st;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    m_ref[g] = -INFINITY;
-    l_run[g] = 0.0f;
+    st.m_ref[g] = -INFINITY;
+    st.l_run[g] = 0.0f;
 #pragma unroll
-    for (int e = 0; e < PE; ++e) acc[g][e] = 0.0f;
+    for (int e = 0; e < PE; ++e) st.acc[g][e] = 0.0f;
   }
   const int tok = lane / LPT;   // QK: token of this lane within a sub-step
   const int part = lane % LPT;  // QK: which slice of the row
   // Query slice in registers, pre-scaled into the log2 domain.  Load i of a
   // lane reads vector part + LPT * ((i + tok) % NV) of the row: rotating by
   // the token spreads one sub-step's tokens over all shared-memory banks.
-  float qr[G][NV][EPV];
   {
     const size_t qrow = (static_cast<size_t>(row) * p.Hq + static_cast<size_t>(h) * G) * D;
 #pragma unroll
@@ -382,132 +491,52 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int vidx = part + LPT * ((i + tok) % NV);
-        load_q_vec<EPV>(p.q, q_bf16, qrow + static_cast<size_t>(g) * D + vidx * EPV, qr[g][i]);
+        load_q_vec<EPV>(p.q, q_bf16, qrow + static_cast<size_t>(g) * D + vidx * EPV, st.qr[g][i]);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) qr[g][i][e] = __fmul_rn(qr[g][i][e], p.qk_scale_log2);
+        for (int e = 0; e < EPV; ++e) st.qr[g][i][e] = __fmul_rn(st.qr[g][i][e], p.qk_scale_log2);
       }
   }
   float* pbuf = &hdr->p[warp][0][0];
-  const int pv_tok = lane / PLT;           // P.V: token of this lane within an iteration
+  const int pv_tok = lane / PLT;              // P.V: token of this lane within an iteration
   const int pv_off = (lane % PLT) * Geo::VB;  // P.V: byte offset of this lane's elements
+  const int wtok0 = warp * WT;                // this warp's first token in a stage
 
+  int s = 0;         // ring slot of stage n
+  uint32_t ph = 0;   // phase parity of that slot's current use
   for (int n = 0; n < nstage && !unit_bad; ++n) {
-    const int s = n % nst;
-    bool got = mbar_wait(&hdr->full[s], (n / nst) & 1, p.wait_limit);
+    bool got = mbar_wait(&hdr->full[s], ph, p.wait_limit);
     if (p.debug_stall) got = got && mbar_wait(&hdr->stall, 0, p.wait_limit);  // runs out by construction
-    const bool landed = __all_sync(0xffffffffu, got);
-    if (!landed) {
+    if (!__all_sync(0xffffffffu, got)) {
       if (lane == 0) {
         record_error(p.status, ST_TIMEOUT);
         hdr->bad = 1;
       }
       break;
     }
-    const unsigned char* ks = ring + static_cast<size_t>(s) * 2 * ST * RB;
+    const unsigned char* ks = ring + static_cast<size_t>(s) * 2 * ST * RB + static_cast<size_t>(wtok0) * RB;
     const unsigned char* vs = ks + ST * RB;
-    const int wtok0 = warp * WT;  // this warp's first token in the stage
     const int n_valid = min(WT, t_end - (t_begin + n * ST + wtok0));
-    if (n_valid > 0) {
-      // ---- scores of the warp's WT tokens (log2 domain), U sub-steps of TPS tokens
-      float sc[U][G];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const unsigned char* krow = ks + static_cast<size_t>(wtok0 + u * TPS + tok) * RB;
-        float partial[G][NV];
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-          const int vidx = part + LPT * ((i + tok) % NV);
-          float kf[EPV];
-          load_widen<KVT, Geo::VEC>(krow + vidx * Geo::VEC, kf);
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            // even and odd elements in the two halves of a packed FMA, then added
-            float2 a = __fmul2_rn(make_float2(qr[g][i][0], qr[g][i][1]), make_float2(kf[0], kf[1]));
-#pragma unroll
-            for (int e = 2; e < EPV; e += 2)
-              a = __ffma2_rn(make_float2(qr[g][i][e], qr[g][i][e + 1]), make_float2(kf[e], kf[e + 1]), a);
-            partial[g][i] = __fadd_rn(a.x, a.y);
-          }
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float a = partial[g][0];
-#pragma unroll
-          for (int i = 1; i < NV; ++i) a = __fadd_rn(a, partial[g][i]);
-#pragma unroll
-          for (int off = 1; off < LPT; off <<= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, off));
-          sc[u][g] = (u * TPS + tok < n_valid) ? a : -INFINITY;
-        }
-      }
-      // ---- online softmax: one reference-max update per stage.  The reference
-      // only moves when the new maximum exceeds it by more than kRescaleSlack
-      // (log2 units), so weights stay <= 2^kRescaleSlack and rescaling is rare.
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float mx = sc[0][g];
-#pragma unroll
-        for (int u = 1; u < U; ++u) mx = fmaxf(mx, sc[u][g]);
-#pragma unroll
-        for (int off = LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        if (mx > __fadd_rn(m_ref[g], kRescaleSlack)) {
-          const float alpha = ex2(__fsub_rn(m_ref[g], mx));
-          m_ref[g] = mx;
-          l_run[g] = __fmul_rn(l_run[g], alpha);
-#pragma unroll
-          for (int e = 0; e < PE; e += 2) {
-            const float2 a = __fmul2_rn(make_float2(acc[g][e], acc[g][e + 1]), make_float2(alpha, alpha));
-            acc[g][e] = a.x;
-            acc[g][e + 1] = a.y;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {  // scores become weights in place
-          sc[u][g] = (u * TPS + tok < n_valid) ? ex2(__fsub_rn(sc[u][g], m_ref[g])) : 0.0f;
-          l_run[g] = __fadd_rn(l_run[g], sc[u][g]);
-        }
-      }
-      __syncwarp();
-      if (part == 0) {
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-          for (int g = 0; g < G; ++g) pbuf[(u * TPS + tok) * 8 + g] = sc[u][g];
-      }
-      __syncwarp();
-      // ---- acc += p . V over the warp's valid tokens, TPV tokens per iteration
-#pragma unroll
-      for (int it = 0; it < NPV; ++it) {
-        const int t = it * TPV + pv_tok;
-        if (t < n_valid) {
-          float vf[PE];
-          load_widen<KVT, Geo::VB>(vs + static_cast<size_t>(wtok0 + t) * RB + pv_off, vf);
-          float pv[G];
-          load_p<G>(pbuf + t * 8, pv);
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int e = 0; e < PE; e += 2) {
-              const float2 a = __ffma2_rn(make_float2(pv[g], pv[g]), make_float2(vf[e], vf[e + 1]),
-                                          make_float2(acc[g][e], acc[g][e + 1]));
-              acc[g][e] = a.x;
-              acc[g][e + 1] = a.y;
-            }
-        }
-      }
-    }
-    // ---- release the stage; the last warp to finish refills it
+    if (n_valid == WT)
+      decode_stage<D, G, KVT, true>(st, ks, vs, pbuf, WT, tok, part, pv_tok, pv_off);
+    else if (n_valid > 0)
+      decode_stage<D, G, KVT, false>(st, ks, vs, pbuf, n_valid, tok, part, pv_tok, pv_off);
+    // ---- release the slot; the last warp to finish refills it
     __syncwarp();
     if (lane == 0) {
       __threadfence_block();
       if (atomicAdd(&hdr->done[s], 1) == NW - 1) {
         hdr->done[s] = 0;
-        const int nn = n + nst;
+        const int nn = n + NST;
         if (nn < nstage) {
           fence_proxy_async();
-          issue_stage<RB>(p, hdr, ring, nn, nst, t_begin, t_end, j0, h, policy);
+          issue_stage<RB>(p, hdr, ring, nn, s, t_begin, t_end, j0, h, lg_p, policy);
           atomicMax(&hdr->issued, nn + 1);
         }
       }
+    }
+    if (++s == NST) {
+      s = 0;
+      ph ^= 1u;
     }
   }
   // each lane summed only its own tokens: complete l over the token lanes and
@@ -515,18 +544,20 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
 #pragma unroll
   for (int g = 0; g < G; ++g) {
 #pragma unroll
-    for (int off = LPT; off < 32; off <<= 1) l_run[g] = __fadd_rn(l_run[g], __shfl_xor_sync(0xffffffffu, l_run[g], off));
+    for (int off = LPT; off < 32; off <<= 1)
+      st.l_run[g] = __fadd_rn(st.l_run[g], __shfl_xor_sync(0xffffffffu, st.l_run[g], off));
 #pragma unroll
     for (int e = 0; e < PE; ++e)
 #pragma unroll
-      for (int off = PLT; off < 32; off <<= 1) acc[g][e] = __fadd_rn(acc[g][e], __shfl_xor_sync(0xffffffffu, acc[g][e], off));
+      for (int off = PLT; off < 32; off <<= 1)
+        st.acc[g][e] = __fadd_rn(st.acc[g][e], __shfl_xor_sync(0xffffffffu, st.acc[g][e], off));
   }
 
   sync_threads_n<Geo::THREADS>();
   if (tid == 0) {
     // every issued copy must land before the ring is reused (only matters after a timeout)
     const int issued = hdr->issued;
-    for (int n = max(0, issued - nst); n < issued; ++n) mbar_wait(&hdr->full[n % nst], (n / nst) & 1, kDrainWaitLimit);
+    for (int n = max(0, issued - NST); n < issued; ++n) mbar_wait(&hdr->full[n % NST], (n / NST) & 1, kDrainWaitLimit);
   }
   sync_threads_n<Geo::THREADS>();
 
@@ -537,11 +568,11 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
   for (int g = 0; g < G; ++g) {
     if (lane < PLT) {
 #pragma unroll
-      for (int e = 0; e < PE; ++e) red_acc[(warp * G + g) * D + lane * PE + e] = acc[g][e];
+      for (int e = 0; e < PE; ++e) red_acc[(warp * G + g) * D + lane * PE + e] = st.acc[g][e];
     }
     if (lane == 0) {
-      red_ml[(warp * G + g) * 2] = m_ref[g];
-      red_ml[(warp * G + g) * 2 + 1] = l_run[g];
+      red_ml[(warp * G + g) * 2] = st.m_ref[g];
+      red_ml[(warp * G + g) * 2 + 1] = st.l_run[g];
     }
   }
   sync_threads_n<Geo::THREADS>();
@@ -603,7 +634,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
   // shared memory first, so the value loads below are independent and coalesced.
   const size_t slot_base = out_row * p.max_splits;  // slot of (head 0 of the group, split 0)
   float* fbuf = red_acc + NW * G * D + NW * G * 2;   // [G][nsplit] weights, then [G] sums
-  const int ring_floats = p.n_stages * Geo::STAGE_BYTES / 4 - (NW * G * D + NW * G * 2);
+  const int ring_floats = NST * Geo::STAGE_BYTES / 4 - (NW * G * D + NW * G * 2);
   if (G * (nsplit + 1) <= ring_floats) {
     for (int i = tid; i < G * nsplit; i += Geo::THREADS) {
       const int g = i / nsplit, sp = i % nsplit;

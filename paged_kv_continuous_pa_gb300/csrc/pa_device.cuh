@@ -45,25 +45,37 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// One poll of the phase with the given parity.  If the phase is not complete
+// the thread may sleep in the poll for up to kWaitHintNs (the hardware wakes
+// it when the phase completes), so waiting warps do not spin on the issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kWaitHintNs)
       : "memory");
   return ok != 0;
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false
-// if it gave up after `limit` polls (each poll may itself suspend the thread
-// for a short hardware-defined time).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
+// if it has not completed after limit_us microseconds.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit_us) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  const uint64_t limit_ns = static_cast<uint64_t>(limit_us) * 1000u;
+  while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-  return false;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
 }
 
 // ------------------------------------------------------- 1-D bulk copy (TMA) --

@@ -10,8 +10,9 @@ namespace pa {
 
 constexpr int kMaxChunks = 16;          // prefill chunks per pa_attention call
 constexpr int kDefaultSplitTokens = 4096;
-constexpr uint32_t kDefaultWaitLimit = 1u << 22;  // polls of one bounded wait (about a second)
-constexpr uint32_t kDrainWaitLimit = 1u << 22;    // polls spent draining copies on an error path
+constexpr uint32_t kDefaultWaitLimit = 1000000;  // microseconds one bounded wait may take (one second)
+constexpr uint32_t kDrainWaitLimit = 1000000;    // microseconds spent draining copies on an error path
+constexpr uint32_t kWaitHintNs = 10000;          // longest sleep inside one mbarrier poll
 constexpr int kMaxStages = 16;          // decode pipeline depth upper bound
 constexpr int kDecodeWarps = 4;         // warps of a decode CTA
 constexpr int kStageTokens = 32;        // tokens per decode pipeline stage
@@ -72,7 +73,7 @@ struct AttnParams {
   float* ws_ml;          // [n_rows][Hq][max_splits][2] partial (max, sum)
   int32_t* ws_count;     // [n_rows][Hkv] finished-split counters, zero between calls
   int32_t* status;
-  uint32_t wait_limit;
+  uint32_t wait_limit;   // microseconds
   int32_t debug_stall;   // 1: every CTA also waits on a barrier nothing completes (failure-path test)
   int32_t n_stages;      // decode pipeline depth (set per instantiation at launch)
   int32_t n_prefill_ctas;  // CTAs [0, n_prefill_ctas) run prefill tiles, the rest decode units
