@@ -56,14 +56,22 @@ def measured_peaks():
 def profiled_traffic(workload: str, src_hash: str):
     """DRAM bytes per attention launch from the committed ncu summary, if it was
     taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_attention_{workload}.json")
+    path = os.path.join(ROOT, "profiles", f"traffic_decode_attention_{workload}.txt")
     if not os.path.exists(path):
         return None
+    fields = {}
     with open(path) as f:
-        d = json.load(f)
-    if d.get("kernel_source_hash") != src_hash:
+        for line in f:
+            if line.startswith("#") or ":" not in line:
+                continue
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("kernel_source_hash") != src_hash:
         return None
-    return d.get("dram_bytes_per_launch")
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 class ClockSampler:
