@@ -18,7 +18,7 @@ struct pa_pool {
   pa_pool_desc desc;
   void* k;
   void* v;
-  bool maps_ready;   // kmap / vmap encoded (on first use by the tile path)
+  bool maps_ready;   // kmap / vmap encoded (on first use by a tensor-map path)
   CUtensorMap kmap;  // 2-D views of the pools for tensor-map copies
   CUtensorMap vmap;
 };
@@ -137,21 +137,28 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// The pool as a 2-D bf16 tensor [num_pages * Hkv * P rows][D], boxes of 64
-// elements x P rows (one page of one kv head, half or all of the head dim),
-// 128-byte swizzle: the layout the tensor-core tile path reads.
+// The pool as a 2-D tensor [num_pages * Hkv * P rows][D] with 128-byte
+// swizzle, the layout the tensor-core paths read.  bf16 pools (the prefill
+// tile path): boxes of 64 elements x P rows, one page of one kv head, half or
+// all of the head dim.  e4m3 pools with D = 128 (the tensor-core decode
+// units): the rows as 128 bytes, boxes of 128 bytes x min(P, 32) rows.
 pa_status encode_pool_maps(pa_pool* pool) {
   if (pool->maps_ready) return PA_OK;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const pa_pool_desc& d = pool->desc;
+  const bool fp8 = d.kv_dtype == PA_FP8_E4M3;
+  if (!(d.kv_dtype == PA_BF16 || (fp8 && d.head_dim == 128)))
+    return fail(PA_ERR_UNSUPPORTED, "no tensor-map view for this pool's dtype / head_dim");
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim),
                         static_cast<cuuint64_t>(d.num_pages) * d.num_kv_heads * d.page_size};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(d.page_size)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * elt_bytes(d.kv_dtype)};
+  cuuint32_t box[2] = {fp8 ? 128u : 64u,
+                       static_cast<cuuint32_t>(fp8 && d.page_size > 32 ? 32 : d.page_size)};
   cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   for (int i = 0; i < 2; ++i) {
-    CUresult r = enc(i == 0 ? &pool->kmap : &pool->vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, i == 0 ? pool->k : pool->v,
+    CUresult r = enc(i == 0 ? &pool->kmap : &pool->vmap, ty, 2, i == 0 ? pool->k : pool->v,
                      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
@@ -368,10 +375,23 @@ pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dt
     p.n_prefill_ctas = pl.cta_begin[pl.n_tile];
   }
 
+  // e4m3 pools whose query-head group makes Q.K and P.V small contractions:
+  // tensor-core decode units, reading stages through the pool's tensor maps.
+  const bool mma_decode = d.kv_dtype == PA_FP8_E4M3 && p.n_prefill_ctas == 0 &&
+                          pa::decode_e4m3_mma_eligible(d.head_dim, G, q_dtype == PA_BF16);
+  if (mma_decode) {
+    pa_status st = encode_pool_maps(const_cast<pa_pool*>(pool));
+    if (st != PA_OK) return st;
+    p.kmap = pool->kmap;
+    p.vmap = pool->vmap;
+  }
+
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (p.n_prefill_ctas > 0) {
     e = pa::launch_mixed_bf16(p, s);
+  } else if (mma_decode) {
+    e = pa::launch_decode_e4m3_mma(p, s);
   } else {
     switch (d.kv_dtype) {
       case PA_F32: e = pa::launch_decode_f32(p, s); break;

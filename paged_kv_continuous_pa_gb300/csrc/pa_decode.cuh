@@ -390,6 +390,124 @@ __device__ __forceinline__ void decode_stage(DecodeState<G, DecodeGeom<D, G, KVT
   }
 }
 
+// The end of a decode unit, shared by the SIMT and tensor-core units: the NW
+// warps' (max, sum, accumulator) states sit in shared memory as red_ml
+// [NW][G][2] and red_acc [NW][G][D]; they are merged in warp order.  A row
+// with one split writes its output; otherwise each split publishes its
+// partial triple to the workspace and the last split to finish merges all of
+// them in ascending split order (the counter is left at zero for the next
+// call).  ring_bytes: shared memory from red_acc on, for the merge weights.
+template <int D, int G, int KVT, int NW, int THREADS>
+__device__ __forceinline__ void decode_finish(const AttnParams& p, bool bad, int32_t* last_flag, float* red_acc,
+                                              const float* red_ml, size_t out_row, int row, int h, int split,
+                                              int nsplit, bool q_bf16, int ring_bytes) {
+  const int tid = threadIdx.x;
+  if (nsplit == 1) {
+    for (int i = tid; i < G * D; i += THREADS) {
+      const int g = i / D, d = i % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, red_ml[(w * G + g) * 2]);
+      float lsum = 0.0f, osum = 0.0f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float f = ex2(__fsub_rn(red_ml[(w * G + g) * 2], M));
+        lsum = fmaf(f, red_ml[(w * G + g) * 2 + 1], lsum);
+        osum = fmaf(f, red_acc[(w * G + g) * D + d], osum);
+      }
+      float o = __fdiv_rn(osum, lsum);
+      if (KVT == KV_E4M3) o = __fmul_rn(o, p.v_scale);
+      store_out(p.out, q_bf16, out_row * D + i, bad ? 0.0f : o);
+    }
+    return;
+  }
+
+  // ---- split row: publish this split's partial triple, the last split merges
+  for (int i = tid; i < G * D; i += THREADS) {
+    const int g = i / D, d = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, red_ml[(w * G + g) * 2]);
+    float lsum = 0.0f, osum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float f = ex2(__fsub_rn(red_ml[(w * G + g) * 2], M));
+      lsum = fmaf(f, red_ml[(w * G + g) * 2 + 1], lsum);
+      osum = fmaf(f, red_acc[(w * G + g) * D + d], osum);
+    }
+    const size_t slot = (out_row + g) * p.max_splits + split;
+    if (bad) {
+      M = -INFINITY;
+      lsum = 0.0f;
+      osum = 0.0f;
+    }
+    p.ws_o[slot * D + d] = osum;
+    if (d == 0) {
+      p.ws_ml[slot * 2] = M;
+      p.ws_ml[slot * 2 + 1] = lsum;
+    }
+  }
+  __threadfence();
+  sync_threads_n<THREADS>();
+  int32_t* counter = p.ws_count + static_cast<size_t>(row) * p.Hkv + h;
+  if (tid == 0) *last_flag = (atomicAdd(counter, 1) == nsplit - 1) ? 1 : 0;
+  sync_threads_n<THREADS>();
+  if (!*last_flag) return;
+  __threadfence();
+  // Merge the splits in ascending order.  The (max, sum) pairs go through
+  // shared memory first, so the value loads below are independent and coalesced.
+  const size_t slot_base = out_row * p.max_splits;  // slot of (head 0 of the group, split 0)
+  float* fbuf = red_acc + NW * G * D + NW * G * 2;   // [G][nsplit] weights, then [G] sums
+  const int ring_floats = ring_bytes / 4 - (NW * G * D + NW * G * 2);
+  if (G * (nsplit + 1) <= ring_floats) {
+    for (int i = tid; i < G * nsplit; i += THREADS) {
+      const int g = i / nsplit, sp = i % nsplit;
+      fbuf[i] = __ldcg(p.ws_ml + (slot_base + static_cast<size_t>(g) * p.max_splits + sp) * 2);
+    }
+    sync_threads_n<THREADS>();
+    if (tid < G) {
+      const int g = tid;
+      float M = -INFINITY;
+      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, fbuf[g * nsplit + sp]);
+      float lsum = 0.0f;
+      for (int sp = 0; sp < nsplit; ++sp) {
+        const float f = ex2(__fsub_rn(fbuf[g * nsplit + sp], M));
+        fbuf[g * nsplit + sp] = f;
+        lsum = fmaf(f, __ldcg(p.ws_ml + (slot_base + static_cast<size_t>(g) * p.max_splits + sp) * 2 + 1), lsum);
+      }
+      fbuf[G * nsplit + g] = lsum;
+    }
+    sync_threads_n<THREADS>();
+    for (int i = tid; i < G * D; i += THREADS) {
+      const int g = i / D, d = i % D;
+      const float* o = p.ws_o + (slot_base + static_cast<size_t>(g) * p.max_splits) * D + d;
+      float osum = 0.0f;
+#pragma unroll 4
+      for (int sp = 0; sp < nsplit; ++sp) osum = fmaf(fbuf[g * nsplit + sp], __ldcg(o + static_cast<size_t>(sp) * D), osum);
+      float out = __fdiv_rn(osum, fbuf[G * nsplit + g]);
+      if (KVT == KV_E4M3) out = __fmul_rn(out, p.v_scale);
+      store_out(p.out, q_bf16, out_row * D + i, out);
+    }
+  } else {
+    for (int i = tid; i < G * D; i += THREADS) {
+      const int g = i / D, d = i % D;
+      const size_t slot0 = (out_row + g) * p.max_splits;
+      float M = -INFINITY;
+      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(p.ws_ml + (slot0 + sp) * 2));
+      float lsum = 0.0f, osum = 0.0f;
+      for (int sp = 0; sp < nsplit; ++sp) {
+        const float f = ex2(__fsub_rn(__ldcg(p.ws_ml + (slot0 + sp) * 2), M));
+        lsum = fmaf(f, __ldcg(p.ws_ml + (slot0 + sp) * 2 + 1), lsum);
+        osum = fmaf(f, __ldcg(p.ws_o + (slot0 + sp) * D + d), osum);
+      }
+      float out = __fdiv_rn(osum, lsum);
+      if (KVT == KV_E4M3) out = __fmul_rn(out, p.v_scale);
+      store_out(p.out, q_bf16, out_row * D + i, out);
+    }
+  }
+  if (tid == 0) *counter = 0;  // leave the workspace zero-filled for the next call
+}
+
 // ------------------------------------------------------------ the unit --
 
 template <int D, int G, int KVT>
@@ -576,112 +694,9 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
     }
   }
   sync_threads_n<Geo::THREADS>();
-  const bool bad = hdr->bad != 0;
-  const size_t out_row = static_cast<size_t>(row) * p.Hq + static_cast<size_t>(h) * G;
-  if (nsplit == 1) {
-    for (int i = tid; i < G * D; i += Geo::THREADS) {
-      const int g = i / D, d = i % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, red_ml[(w * G + g) * 2]);
-      float lsum = 0.0f, osum = 0.0f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float f = ex2(__fsub_rn(red_ml[(w * G + g) * 2], M));
-        lsum = fmaf(f, red_ml[(w * G + g) * 2 + 1], lsum);
-        osum = fmaf(f, red_acc[(w * G + g) * D + d], osum);
-      }
-      float o = __fdiv_rn(osum, lsum);
-      if (KVT == KV_E4M3) o = __fmul_rn(o, p.v_scale);
-      store_out(p.out, q_bf16, out_row * D + i, bad ? 0.0f : o);
-    }
-    return;
-  }
-
-  // ---- split row: publish this split's partial triple, the last split merges
-  for (int i = tid; i < G * D; i += Geo::THREADS) {
-    const int g = i / D, d = i % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, red_ml[(w * G + g) * 2]);
-    float lsum = 0.0f, osum = 0.0f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float f = ex2(__fsub_rn(red_ml[(w * G + g) * 2], M));
-      lsum = fmaf(f, red_ml[(w * G + g) * 2 + 1], lsum);
-      osum = fmaf(f, red_acc[(w * G + g) * D + d], osum);
-    }
-    const size_t slot = (out_row + g) * p.max_splits + split;
-    if (bad) {
-      M = -INFINITY;
-      lsum = 0.0f;
-      osum = 0.0f;
-    }
-    p.ws_o[slot * D + d] = osum;
-    if (d == 0) {
-      p.ws_ml[slot * 2] = M;
-      p.ws_ml[slot * 2 + 1] = lsum;
-    }
-  }
-  __threadfence();
-  sync_threads_n<Geo::THREADS>();
-  int32_t* counter = p.ws_count + static_cast<size_t>(row) * p.Hkv + h;
-  if (tid == 0) hdr->last = (atomicAdd(counter, 1) == nsplit - 1) ? 1 : 0;
-  sync_threads_n<Geo::THREADS>();
-  if (!hdr->last) return;
-  __threadfence();
-  // Merge the splits in ascending order.  The (max, sum) pairs go through
-  // shared memory first, so the value loads below are independent and coalesced.
-  const size_t slot_base = out_row * p.max_splits;  // slot of (head 0 of the group, split 0)
-  float* fbuf = red_acc + NW * G * D + NW * G * 2;   // [G][nsplit] weights, then [G] sums
-  const int ring_floats = NST * Geo::STAGE_BYTES / 4 - (NW * G * D + NW * G * 2);
-  if (G * (nsplit + 1) <= ring_floats) {
-    for (int i = tid; i < G * nsplit; i += Geo::THREADS) {
-      const int g = i / nsplit, sp = i % nsplit;
-      fbuf[i] = __ldcg(p.ws_ml + (slot_base + static_cast<size_t>(g) * p.max_splits + sp) * 2);
-    }
-    sync_threads_n<Geo::THREADS>();
-    if (tid < G) {
-      const int g = tid;
-      float M = -INFINITY;
-      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, fbuf[g * nsplit + sp]);
-      float lsum = 0.0f;
-      for (int sp = 0; sp < nsplit; ++sp) {
-        const float f = ex2(__fsub_rn(fbuf[g * nsplit + sp], M));
-        fbuf[g * nsplit + sp] = f;
-        lsum = fmaf(f, __ldcg(p.ws_ml + (slot_base + static_cast<size_t>(g) * p.max_splits + sp) * 2 + 1), lsum);
-      }
-      fbuf[G * nsplit + g] = lsum;
-    }
-    sync_threads_n<Geo::THREADS>();
-    for (int i = tid; i < G * D; i += Geo::THREADS) {
-      const int g = i / D, d = i % D;
-      const float* o = p.ws_o + (slot_base + static_cast<size_t>(g) * p.max_splits) * D + d;
-      float osum = 0.0f;
-#pragma unroll 4
-      for (int sp = 0; sp < nsplit; ++sp) osum = fmaf(fbuf[g * nsplit + sp], __ldcg(o + static_cast<size_t>(sp) * D), osum);
-      float out = __fdiv_rn(osum, fbuf[G * nsplit + g]);
-      if (KVT == KV_E4M3) out = __fmul_rn(out, p.v_scale);
-      store_out(p.out, q_bf16, out_row * D + i, out);
-    }
-  } else {
-    for (int i = tid; i < G * D; i += Geo::THREADS) {
-      const int g = i / D, d = i % D;
-      const size_t slot0 = (out_row + g) * p.max_splits;
-      float M = -INFINITY;
-      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(p.ws_ml + (slot0 + sp) * 2));
-      float lsum = 0.0f, osum = 0.0f;
-      for (int sp = 0; sp < nsplit; ++sp) {
-        const float f = ex2(__fsub_rn(__ldcg(p.ws_ml + (slot0 + sp) * 2), M));
-        lsum = fmaf(f, __ldcg(p.ws_ml + (slot0 + sp) * 2 + 1), lsum);
-        osum = fmaf(f, __ldcg(p.ws_o + (slot0 + sp) * D + d), osum);
-      }
-      float out = __fdiv_rn(osum, lsum);
-      if (KVT == KV_E4M3) out = __fmul_rn(out, p.v_scale);
-      store_out(p.out, q_bf16, out_row * D + i, out);
-    }
-  }
-  if (tid == 0) *counter = 0;  // leave the workspace zero-filled for the next call
+  decode_finish<D, G, KVT, NW, Geo::THREADS>(p, hdr->bad != 0, &hdr->last, red_acc, red_ml,
+                                             static_cast<size_t>(row) * p.Hq + static_cast<size_t>(h) * G, row, h,
+                                             split, nsplit, q_bf16, NST * Geo::STAGE_BYTES);
 }
 
 template <int D, int G, int KVT>

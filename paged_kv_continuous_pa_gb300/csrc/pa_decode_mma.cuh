@@ -1,0 +1,440 @@
+// pa_decode_mma.cuh -- decode units for FP8 (E4M3) K/V pools with head_dim 128,
+// where the query-head group makes Q.K and P.V a small dense contraction
+// (G query heads x 32 keys x 128 per stage): warp-level tensor-core MMAs
+// (mma.sync m16n8k16, f16 inputs, FP32 accumulation) instead of FP32 FMAs.
+//
+// Why: with G = 7 query heads per KV head ("Engines for the card you have":
+// a 7B model with an FP8 key/value cache), each K/V byte feeds 7 FMAs; at HBM
+// rate that is more than the FP32 pipes deliver, so the SIMT decode path is
+// compute-bound here.  The tensor cores make the arithmetic cheap; what is
+// left per byte is one conversion (e4m3x2 -> f16x2, exact).
+//
+// Same contract and CTA shape as the SIMT decode unit (4 warps, one CTA per
+// (row, kv head, split), the same split merge and epilogue), with these
+// differences:
+//   * Stages of 32 tokens arrive by 2-D tensor-map copies (box: 128 bytes x
+//     min(P, 32) rows of one page of one kv head) into 128-byte swizzled
+//     shared-memory tiles, so that ldmatrix and 16-byte row loads are free of
+//     bank conflicts.  Warp w consumes stages w, w + 4, ... whole.  The ring
+//     has 8 slots and slot s belongs to warp s % 4: a warp refills the slot it
+//     has just finished and is the only one to wait on it, so every wait is on
+//     the slot's current or next phase.
+//   * S^T = K . Q^T: A = K (16 keys x 16 head elements) from ldmatrix on the fp8
+//     bytes; each 32-bit fragment word holds 4 consecutive fp8 elements, so the
+//     two f16x2 conversions of a word feed two MMAs whose k order is permuted;
+//     the query fragments (B, constant per unit) are laid out with the same
+//     permutation.  Query heads are the MMA's n (8; heads >= G are zero).
+//   * O^T += V^T . P^T: A = V^T (16 head elements x 16 keys) built from 16-byte
+//     row loads with byte permutes and e4m3x2 -> f16x2 conversions; thread t
+//     owns head elements 16 (t/4) .. 16 (t/4) + 15, so the MMA's m rows are a
+//     fixed permutation of the head dim, undone when the accumulators are
+//     written out.  B = P^T: the softmax weights, rounded to f16 (weights are
+//     <= 2^8 by the lazy reference max), moved into fragment order with
+//     movmatrix.trans.
+//   * The query enters as f16, scaled by a power of two chosen per (row, kv
+//     head) so that its largest element is below 2^15; the power is folded
+//     back into the score scale.  bf16 values in the f16 normal range are exact.
+//   * Value rows of keys past the row's position in the last stage are zeroed in
+//     shared memory before P.V (zero weights must never meet stale or NaN bytes).
+#pragma once
+
+#include "pa_decode.cuh"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+
+// ------------------------------------------------------- warp-level MMA --
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* smem_row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(smem_row)));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// Two e4m3 codes in the low (lo = true) or high half of w -> f16x2, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w, bool lo) {
+  uint32_t d;
+  if (lo)
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}" : "=r"(d) : "r"(w));
+  else
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(d) : "r"(w));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Byte i of the 16-byte swizzled row r of a 128-byte-per-row tile: chunk c sits
+// at chunk position c ^ (r % 8).
+__device__ __forceinline__ uint32_t sw128(int r, int chunk) { return r * 128 + ((chunk ^ (r & 7)) << 4); }
+
+constexpr int kMmaStageBytes = 2 * kStageTokens * 128;  // K and V rows of one stage
+
+struct MmaSmemHeader {
+  uint64_t full[kMaxStages];   // stage landed (tensor-map copy bytes)
+  uint64_t stall;              // never completed: the injected-stall test waits here
+  int32_t bad;                 // a page id was out of range or a wait gave up
+  int32_t last;                // this CTA merges the splits of its (row, kv head)
+  int32_t pid[kMaxUnitPages];  // the unit's physical page ids
+};
+
+__host__ __device__ constexpr size_t mma_header_bytes() { return (sizeof(MmaSmemHeader) + 1023) / 1024 * 1024; }
+
+template <int G>
+struct MmaGeom {
+  static constexpr int D = 128;
+  static constexpr int NW = kDecodeWarps;
+  static constexpr int THREADS = NW * 32;
+  static constexpr int STAGES = 8;  // two slots per warp, 64 KiB of ring: three CTAs per SM
+  static constexpr int MIN_CTAS = 3;
+  static_assert(STAGES % NW == 0 && STAGES <= kMaxStages, "a slot belongs to one warp");
+  static_assert(G >= 1 && G <= 8, "query heads per kv head");
+};
+
+// Copy the token slots of stage n (32 tokens from t_begin + 32 n) into ring
+// slot s by tensor-map boxes of BR = min(P, 32) rows; every box is whole, so
+// the last stage may carry slots past the unit's end (masked / zeroed later).
+__device__ __forceinline__ void mma_issue_stage(const AttnParams& p, MmaSmemHeader* hdr, unsigned char* ring, int n,
+                                                int s, int t_begin, int t_end, int j0, int h, int lg_p) {
+  const int a = t_begin + n * kStageTokens;
+  const int b = min(t_end, a + kStageTokens);
+  const int P = 1 << lg_p;
+  const int BR = P < kStageTokens ? P : kStageTokens;
+  unsigned char* ks = ring + static_cast<size_t>(s) * kMmaStageBytes;
+  unsigned char* vs = ks + kStageTokens * 128;
+  const int nbox = (b - a + BR - 1) / BR;
+  mbar_arrive_expect_tx(&hdr->full[s], static_cast<uint32_t>(2 * nbox * BR * 128));
+  for (int k = 0; k < nbox; ++k) {
+    const int t = a + k * BR;
+    const int page = hdr->pid[(t >> lg_p) - j0];
+    const int y = (page * p.Hkv + h) * P + (t & (P - 1));
+    tc::tma_load_2d(ks + k * BR * 128, &p.kmap, 0, y, &hdr->full[s]);
+    tc::tma_load_2d(vs + k * BR * 128, &p.vmap, 0, y, &hdr->full[s]);
+  }
+}
+
+template <int G>
+__device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, unsigned char* smem_raw) {
+  using Geo = MmaGeom<G>;
+  constexpr int D = 128, NW = Geo::NW, NST = Geo::STAGES, ST = kStageTokens;
+
+  const int h = unit % p.Hkv;
+  const int rest = unit / p.Hkv;
+  const int split = rest % p.max_splits;
+  const int row = rest / p.max_splits;
+  if (row >= p.n_rows) return;
+  if (p.n_chunks > 0 && row_in_chunk(p, row)) return;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int seq = __ldg(p.seq_ids + row);
+  const int pos = __ldg(p.positions + row);
+  const bool q_bf16 = p.q_is_bf16 != 0;
+  const int P = p.P;
+  const size_t out_row = static_cast<size_t>(row) * p.Hq + static_cast<size_t>(h) * G;
+
+  if (seq < 0 || seq >= p.num_seqs || pos < 0 || pos >= p.max_blocks * P) {
+    if (split == 0) {
+      for (int i = tid; i < G * D; i += Geo::THREADS) store_out(p.out, q_bf16, out_row * D + i, 0.0f);
+      if (tid == 0) record_error(p.status, ST_OUT_OF_RANGE);
+    }
+    return;
+  }
+  const int L = pos + 1;
+  const int nsplit = (L + p.split_tokens - 1) / p.split_tokens;
+  if (split >= nsplit) return;
+  const int t_begin = split * p.split_tokens;
+  const int t_end = min(L, t_begin + p.split_tokens);
+  const int j0 = t_begin / P;
+  const int npg = (t_end + P - 1) / P - j0;
+  const int nstage = (t_end - t_begin + ST - 1) / ST;
+  const int lg_p = 31 - __clz(P);
+
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  MmaSmemHeader* hdr = reinterpret_cast<MmaSmemHeader*>(smem);
+  unsigned char* ring = smem + mma_header_bytes();
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(&hdr->full[s], 1);
+    mbar_init(&hdr->stall, 1);
+    hdr->bad = 0;
+    hdr->last = 0;
+    fence_barrier_init();
+  }
+  {
+    const int32_t* bt = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + j0;
+    bool bad = false;
+    for (int i = tid; i < npg && i < kMaxUnitPages; i += Geo::THREADS) {
+      const int pid = __ldg(bt + i);
+      bad |= pid < 0 || pid >= p.num_pages;
+      hdr->pid[i] = pid;
+    }
+    sync_threads_n<Geo::THREADS>();
+    if (bad) {
+      hdr->bad = 1;
+      record_error(p.status, ST_OUT_OF_RANGE);
+    }
+  }
+  sync_threads_n<Geo::THREADS>();
+  const bool unit_bad = hdr->bad != 0;
+  if (tid == 0 && !unit_bad) {
+    const int first = min(NST, nstage);
+    for (int n = 0; n < first; ++n) mma_issue_stage(p, hdr, ring, n, n, t_begin, t_end, j0, h, lg_p);
+  }
+
+  const int g4 = lane >> 2;  // fragment group: key row (QK), head element block (PV), query head (B operand)
+  const int t4 = lane & 3;   // thread in group
+
+  // ---- query fragments (B of Q.K), f16, in the permuted k order of the K fragments:
+  // for head block kb (32 elements) the first MMA reads elements 32kb + 4 t4 + {0,1}
+  // and 32kb + 16 + 4 t4 + {0,1}, the second + 2.  Head g4 of the group (zero if >= G).
+  uint32_t qf[4][4];  // [kb][mma0 b0, mma0 b1, mma1 b0, mma1 b1]
+  float score_scale;
+  {
+    float qv[4][8];
+    float amax = 0.0f;
+    const bool head_ok = g4 < G;
+    const size_t qoff = (out_row + (head_ok ? g4 : 0)) * D;
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+      float f[4];
+      load_q_vec<4>(p.q, q_bf16, qoff + 32 * kb + 4 * t4, f);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qv[kb][i] = head_ok ? f[i] : 0.0f;
+      load_q_vec<4>(p.q, q_bf16, qoff + 32 * kb + 16 + 4 * t4, f);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qv[kb][4 + i] = head_ok ? f[i] : 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(qv[kb][i]));
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    // Scale by 2^-shift so that the largest element lands in [2^14, 2^15):
+    // amax = 1.f * 2^(E - 127) for biased exponent E; subnormal or zero
+    // queries take the clamp.
+    const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 126;
+    const int shift = min(100, max(-100, e - 15));
+    const float down = __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
+    score_scale = __fmul_rn(p.qk_scale_log2, __uint_as_float(static_cast<uint32_t>(127 + shift) << 23));
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+      qf[kb][0] = pack_f16x2(qv[kb][0] * down, qv[kb][1] * down);  // mma0: elements 4t4 + {0,1}
+      qf[kb][1] = pack_f16x2(qv[kb][4] * down, qv[kb][5] * down);  //       16 + 4t4 + {0,1}
+      qf[kb][2] = pack_f16x2(qv[kb][2] * down, qv[kb][3] * down);  // mma1: 4t4 + {2,3}
+      qf[kb][3] = pack_f16x2(qv[kb][6] * down, qv[kb][7] * down);  //       16 + 4t4 + {2,3}
+    }
+  }
+
+  // ---- per-warp state: heads 2 t4 and 2 t4 + 1; O^T rows d(i, g4) = 16 g4 + i and
+  // d(i, g4 + 8) = 16 g4 + 8 + i for m-tile i
+  float m_ref[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+
+  int drain_n = -1;  // the stage a wait gave up on
+  for (int n = warp; n < nstage && !unit_bad; n += NW) {
+    const int s = n % NST;
+    bool got = mbar_wait(&hdr->full[s], (n / NST) & 1, p.wait_limit);
+    if (p.debug_stall) got = got && mbar_wait(&hdr->stall, 0, p.wait_limit);  // runs out by construction
+    if (!__all_sync(0xffffffffu, got)) {
+      if (lane == 0) {
+        record_error(p.status, ST_TIMEOUT);
+        hdr->bad = 1;
+      }
+      drain_n = n;
+      break;
+    }
+    unsigned char* ks = ring + static_cast<size_t>(s) * kMmaStageBytes;
+    unsigned char* vs = ks + ST * 128;
+    const int n_valid = min(ST, t_end - (t_begin + n * ST));  // 1..32
+    // ---- S^T = K . Q^T for the stage's two 16-key m-tiles
+    float sc[2][4];
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi) {
+      sc[mi][0] = sc[mi][1] = sc[mi][2] = sc[mi][3] = 0.0f;
+      const int r = 16 * mi + (lane & 7) + ((lane >> 3) & 1) * 8;  // row this lane addresses for ldmatrix
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) {
+        uint32_t kr[4];
+        ldmatrix_x4(kr, ks + sw128(r, 2 * kb + (lane >> 4)));
+        const uint32_t a0[4] = {e4m3x2_to_f16x2(kr[0], true), e4m3x2_to_f16x2(kr[1], true),
+                                e4m3x2_to_f16x2(kr[2], true), e4m3x2_to_f16x2(kr[3], true)};
+        const uint32_t a1[4] = {e4m3x2_to_f16x2(kr[0], false), e4m3x2_to_f16x2(kr[1], false),
+                                e4m3x2_to_f16x2(kr[2], false), e4m3x2_to_f16x2(kr[3], false)};
+        mma_f16_16816(sc[mi], a0, qf[kb][0], qf[kb][1]);
+        mma_f16_16816(sc[mi], a1, qf[kb][2], qf[kb][3]);
+      }
+    }
+    // ---- online softmax: this lane holds keys 16 mi + g4 (+8) for heads 2 t4 (+1)
+    const bool full = n_valid == ST;
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int key = 16 * mi + g4 + (c >> 1) * 8;
+        sc[mi][c] = (full || key < n_valid) ? __fmul_rn(sc[mi][c], score_scale) : -INFINITY;
+      }
+    uint32_t pb[2][2];  // P^T fragments: [k-step][keys 0..7 / 8..15 of it]
+    float alpha2[2];
+    bool rescale = false;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float mx = fmaxf(fmaxf(sc[0][hh], sc[0][2 + hh]), fmaxf(sc[1][hh], sc[1][2 + hh]));
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      alpha2[hh] = 1.0f;
+      if (mx > __fadd_rn(m_ref[hh], kRescaleSlack)) {
+        alpha2[hh] = ex2(__fsub_rn(m_ref[hh], mx));
+        rescale = true;
+        m_ref[hh] = mx;
+        l_run[hh] = __fmul_rn(l_run[hh], alpha2[hh]);
+      }
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const float v = sc[mi][2 * c2 + hh];
+          const float w = v == -INFINITY ? 0.0f : ex2(__fsub_rn(v, m_ref[hh]));
+          sc[mi][2 * c2 + hh] = w;
+          l_run[hh] = __fadd_rn(l_run[hh], w);
+        }
+    }
+    if (__any_sync(0xffffffffu, rescale)) {  // rare: the reference maximum moved
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        o[i][0] = __fmul_rn(o[i][0], alpha2[0]);
+        o[i][1] = __fmul_rn(o[i][1], alpha2[1]);
+        o[i][2] = __fmul_rn(o[i][2], alpha2[0]);
+        o[i][3] = __fmul_rn(o[i][3], alpha2[1]);
+      }
+    }
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi) {
+      // C layout (key g4 / g4+8, heads 2t4, 2t4+1) -> B layout (head g4, keys 2t4, 2t4+1)
+      pb[mi][0] = movmatrix_trans(pack_f16x2(sc[mi][0], sc[mi][1]));
+      pb[mi][1] = movmatrix_trans(pack_f16x2(sc[mi][2], sc[mi][3]));
+    }
+    // ---- value rows past the row's position: zero them before they meet weight 0
+    if (!full) {
+      for (int i = lane; i < (ST - n_valid) * 8; i += 32)
+        *reinterpret_cast<uint4*>(vs + (n_valid + i / 8) * 128 + (i % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
+    }
+    // ---- O^T += V^T . P^T, two 16-key k-steps
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi) {
+      const int ta = 16 * mi + 2 * t4;  // keys ta, ta+1 (k slots 2t4, 2t4+1) and ta+8, ta+9
+      const uint4 va = *reinterpret_cast<const uint4*>(vs + sw128(ta, g4));
+      const uint4 vb = *reinterpret_cast<const uint4*>(vs + sw128(ta + 1, g4));
+      const uint4 vc = *reinterpret_cast<const uint4*>(vs + sw128(ta + 8, g4));
+      const uint4 vd = *reinterpret_cast<const uint4*>(vs + sw128(ta + 9, g4));
+      const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+      const uint32_t wc[4] = {vc.x, vc.y, vc.z, vc.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {  // head elements 4w .. 4w+3 (rows g4) and 8 + 4w .. (rows g4 + 8)
+        // byte pairs (key ta, key ta+1) and (ta+8, ta+9) for element e: low byte from the first key
+        const uint32_t ab_lo = __byte_perm(wa[w], wb[w], 0x5140), ab_hi = __byte_perm(wa[w], wb[w], 0x7362);
+        const uint32_t ab8_lo = __byte_perm(wa[w + 2], wb[w + 2], 0x5140), ab8_hi = __byte_perm(wa[w + 2], wb[w + 2], 0x7362);
+        const uint32_t cd_lo = __byte_perm(wc[w], wd[w], 0x5140), cd_hi = __byte_perm(wc[w], wd[w], 0x7362);
+        const uint32_t cd8_lo = __byte_perm(wc[w + 2], wd[w + 2], 0x5140), cd8_hi = __byte_perm(wc[w + 2], wd[w + 2], 0x7362);
+        // element 4w + j of the thread's 16: m-tile i = 4w + j
+        const uint32_t a_j0[4] = {e4m3x2_to_f16x2(ab_lo, true), e4m3x2_to_f16x2(ab8_lo, true),
+                                  e4m3x2_to_f16x2(cd_lo, true), e4m3x2_to_f16x2(cd8_lo, true)};
+        const uint32_t a_j1[4] = {e4m3x2_to_f16x2(ab_lo, false), e4m3x2_to_f16x2(ab8_lo, false),
+                                  e4m3x2_to_f16x2(cd_lo, false), e4m3x2_to_f16x2(cd8_lo, false)};
+        const uint32_t a_j2[4] = {e4m3x2_to_f16x2(ab_hi, true), e4m3x2_to_f16x2(ab8_hi, true),
+                                  e4m3x2_to_f16x2(cd_hi, true), e4m3x2_to_f16x2(cd8_hi, true)};
+        const uint32_t a_j3[4] = {e4m3x2_to_f16x2(ab_hi, false), e4m3x2_to_f16x2(ab8_hi, false),
+                                  e4m3x2_to_f16x2(cd_hi, false), e4m3x2_to_f16x2(cd8_hi, false)};
+        mma_f16_16816(o[4 * w + 0], a_j0, pb[mi][0], pb[mi][1]);
+        mma_f16_16816(o[4 * w + 1], a_j1, pb[mi][0], pb[mi][1]);
+        mma_f16_16816(o[4 * w + 2], a_j2, pb[mi][0], pb[mi][1]);
+        mma_f16_16816(o[4 * w + 3], a_j3, pb[mi][0], pb[mi][1]);
+      }
+    }
+    // ---- release: this warp was the slot's only reader; refill it
+    __syncwarp();
+    if (lane == 0 && n + NST < nstage) {
+      fence_proxy_async();
+      mma_issue_stage(p, hdr, ring, n + NST, s, t_begin, t_end, j0, h, lg_p);
+    }
+  }
+  // After a wait gave up on stage n, stages n and n + 4 (if any) may still be
+  // in flight into this warp's slots: let them land before the ring is reused.
+  if (drain_n >= 0 && lane == 0) {
+    mbar_wait(&hdr->full[drain_n % NST], (drain_n / NST) & 1, kDrainWaitLimit);
+    const int n2 = drain_n + NW;
+    if (n2 < nstage) mbar_wait(&hdr->full[n2 % NST], (n2 / NST) & 1, kDrainWaitLimit);
+  }
+  // complete each head's sum over the lanes that hold its other keys
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) l_run[hh] = __fadd_rn(l_run[hh], __shfl_xor_sync(0xffffffffu, l_run[hh], off));
+
+  sync_threads_n<Geo::THREADS>();
+
+  // ---- the 4 warps' states to shared memory in the SIMT unit's layout, then
+  // the same fixed-order merges and epilogue
+  float* red_acc = reinterpret_cast<float*>(ring);  // [NW][G][D]
+  float* red_ml = red_acc + NW * G * D;             // [NW][G][2]
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int head = 2 * t4 + hh;
+    if (head < G) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        red_acc[(warp * G + head) * D + 16 * g4 + i] = o[i][hh];
+        red_acc[(warp * G + head) * D + 16 * g4 + 8 + i] = o[i][2 + hh];
+      }
+      if (g4 == 0) {
+        red_ml[(warp * G + head) * 2] = m_ref[hh];
+        red_ml[(warp * G + head) * 2 + 1] = l_run[hh];
+      }
+    }
+  }
+  sync_threads_n<Geo::THREADS>();
+  decode_finish<D, G, KV_E4M3, NW, Geo::THREADS>(p, hdr->bad != 0, &hdr->last, red_acc, red_ml, out_row, row, h,
+                                               split, nsplit, q_bf16, NST * kMmaStageBytes);
+}
+
+template <int G>
+__global__ void __launch_bounds__(MmaGeom<G>::THREADS, MmaGeom<G>::MIN_CTAS) decode_mma_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];  // aligned to 1024 by hand below
+  decode_unit_mma<G>(p, static_cast<int>(blockIdx.x), smem);
+}
+
+constexpr size_t mma_smem_bytes() { return 1024 + mma_header_bytes() + MmaGeom<1>::STAGES * kMmaStageBytes; }
+
+template <int G>
+cudaError_t launch_decode_mma_inst(const AttnParams& p, cudaStream_t stream) {
+  const size_t smem = mma_smem_bytes();
+  static int attr_bytes = 0;
+  if (static_cast<int>(smem) > attr_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_bytes = static_cast<int>(smem);
+  }
+  const long long units = static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
+  if (units <= 0) return cudaSuccess;
+  decode_mma_kernel<G><<<static_cast<unsigned>(units), MmaGeom<G>::THREADS, smem, stream>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -89,7 +89,8 @@ struct AttnParams {
   float* ws_tile_ml;                      // [chunk rows][Hq][tile_splits][2] partial (max, sum)
   int32_t* ws_tile_count;                 // [tiles] finished-split counters, zero between calls
   float sm_scale_log2;                    // softmax scale * log2(e) for the tile path
-  CUtensorMap kmap;                       // K pool as [num_pages * Hkv * P][D] bf16, box 64 x P, 128B swizzle
+  CUtensorMap kmap;                       // bf16 K pool as [num_pages * Hkv * P][D], box 64 x P, 128B swizzle;
+                                          // e4m3 pool (D = 128): bytes [num_pages * Hkv * P][128], box 128 x min(P, 32)
   CUtensorMap vmap;                       // V pool, same geometry
 };
 
@@ -106,6 +107,12 @@ void set_last_error(const char* fmt, ...);
 cudaError_t launch_decode_f32(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_decode_e4m3(const AttnParams& p, cudaStream_t stream);
+
+// Tensor-core decode units for e4m3 pools, head_dim 128, bf16 queries,
+// 3..8 query heads per kv head; p.kmap / p.vmap must be the pools' byte views
+// [num_pages * Hkv * P][128], box 128 x min(P, 32), 128-byte swizzle.
+bool decode_e4m3_mma_eligible(int D, int G, bool q_bf16);
+cudaError_t launch_decode_e4m3_mma(const AttnParams& p, cudaStream_t stream);
 
 // One launch whose first p.n_prefill_ctas CTAs run tensor-core prefill tiles
 // (bf16 q and K/V) and whose remaining CTAs run decode units.
