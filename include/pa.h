@@ -35,7 +35,7 @@
  *
  * Layouts (row-major, innermost last):
  *   k_pool, v_pool   [num_pages][Hkv][P][D]     kv_dtype, 16-byte aligned
- *   q, out           [n_rows][Hq][D]            q_dtype (out has q's dtype)
+ *   q, out           [n_rows][Hq][D]            q_dtype (out has q's dtype), 16-byte aligned
  *   k_new, v_new     [n_rows][Hkv][D]           in_dtype
  *   seq_ids, positions [n_rows]                 int32
  *   block_tables     [num_seqs][max_blocks_per_seq] int32, unused entries -1
@@ -142,8 +142,10 @@ size_t pa_attention_workspace_bytes(const pa_pool *pool, int32_t n_rows, int32_t
  * included, so append the step's rows first).  A row's output bits depend only
  * on that row's inputs and on the rows of its own chunk, never on the other
  * rows of the call or the physical placement of its pages.
- * One launch on `stream` (a second, tiny launch only when a chunk row's
- * attention is split); no allocation; graph-capturable. */
+ * One launch on `stream` (split partials are merged inside it); no allocation;
+ * graph-capturable.  Errors: PA_ERR_INVALID_ARG (NULL or misaligned pointer,
+ * bad sizes, overlapping chunks, workspace too small), PA_ERR_UNSUPPORTED (a
+ * group size or head_dim without a kernel), PA_ERR_CUDA (a failed launch). */
 pa_status pa_attention(const pa_pool *pool, int32_t n_rows, const void *q, pa_dtype q_dtype,
                        int32_t num_q_heads, const int32_t *seq_ids, const int32_t *positions,
                        const int32_t *block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,

@@ -302,6 +302,7 @@ pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dt
   if (n_rows == 0) return PA_OK;
   if (!q || !seq_ids || !positions || !block_tables || !out)
     return fail(PA_ERR_INVALID_ARG, "attention: a device pointer is NULL");
+  if (!aligned(q, 16) || !aligned(out, 16)) return fail(PA_ERR_INVALID_ARG, "q / out must be 16-byte aligned");
   const Plan pl = make_plan(d, n_rows, num_q_heads, max_blocks_per_seq, chunks, n_chunks,
                             q_dtype == PA_BF16 && d.kv_dtype == PA_BF16);
   if (pl.total > 0) {

@@ -9,16 +9,17 @@
 // compute-bound here.  The tensor cores make the arithmetic cheap; what is
 // left per byte is one conversion (e4m3x2 -> f16x2, exact).
 //
-// Same contract and CTA shape as the SIMT decode unit (4 warps, one CTA per
-// (row, kv head, split), the same split merge and epilogue), with these
-// differences:
+// Same contract as the SIMT decode unit (one CTA per (row, kv head, split),
+// the same split merge and epilogue), with these differences:
+//   * A CTA is ONE warp.  A unit's work is a short chain (a few stages at the
+//     context lengths of a 7B-class decode batch), so many small CTAs per SM
+//     keep more units' copies in flight than a few wide ones, and no
+//     cross-warp merge is needed.  The warp waits on, consumes and refills
+//     its ring of NST slots in stage order.
 //   * Stages of 32 tokens arrive by 2-D tensor-map copies (box: 128 bytes x
 //     min(P, 32) rows of one page of one kv head) into 128-byte swizzled
 //     shared-memory tiles, so that ldmatrix and 16-byte row loads are free of
-//     bank conflicts.  Warp w consumes stages w, w + 4, ... whole.  The ring
-//     has 8 slots and slot s belongs to warp s % 4: a warp refills the slot it
-//     has just finished and is the only one to wait on it, so every wait is on
-//     the slot's current or next phase.
+//     bank conflicts.
 //   * S^T = K . Q^T: A = K (16 keys x 16 head elements) from ldmatrix on the fp8
 //     bytes; each 32-bit fragment word holds 4 consecutive fp8 elements, so the
 //     two f16x2 conversions of a word feed two MMAs whose k order is permuted;
@@ -79,6 +80,11 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Byte i of the 16-byte swizzled row r of a 128-byte-per-row tile: chunk c sits
 // at chunk position c ^ (r % 8).
 __device__ __forceinline__ uint32_t sw128(int r, int chunk) { return r * 128 + ((chunk ^ (r & 7)) << 4); }
@@ -95,15 +101,17 @@ struct MmaSmemHeader {
 
 __host__ __device__ constexpr size_t mma_header_bytes() { return (sizeof(MmaSmemHeader) + 1023) / 1024 * 1024; }
 
-template <int G>
+// One warp per CTA, one CTA per unit; NST ring slots of one stage each.
+template <int G, int NST>
 struct MmaGeom {
   static constexpr int D = 128;
-  static constexpr int NW = kDecodeWarps;
-  static constexpr int THREADS = NW * 32;
-  static constexpr int STAGES = 8;  // two slots per warp, 64 KiB of ring: three CTAs per SM
-  static constexpr int MIN_CTAS = 3;
-  static_assert(STAGES % NW == 0 && STAGES <= kMaxStages, "a slot belongs to one warp");
+  static constexpr int THREADS = 32;
+  static constexpr int STAGES = NST;
+  static constexpr size_t SMEM = 1024 + mma_header_bytes() + static_cast<size_t>(NST) * kMmaStageBytes;
+  static_assert(NST >= 2 && NST <= kMaxStages, "ring depth");
   static_assert(G >= 1 && G <= 8, "query heads per kv head");
+  // the epilogue's [G][D] accumulator and [G][2] (max, sum) sit in the ring
+  static_assert(static_cast<size_t>(G) * (D + 2) * 4 <= static_cast<size_t>(NST) * kMmaStageBytes, "ring");
 };
 
 // Copy the token slots of stage n (32 tokens from t_begin + 32 n) into ring
@@ -128,10 +136,9 @@ __device__ __forceinline__ void mma_issue_stage(const AttnParams& p, MmaSmemHead
   }
 }
 
-template <int G>
+template <int G, int NST>
 __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, unsigned char* smem_raw) {
-  using Geo = MmaGeom<G>;
-  constexpr int D = 128, NW = Geo::NW, NST = Geo::STAGES, ST = kStageTokens;
+  constexpr int D = 128, ST = kStageTokens;
 
   const int h = unit % p.Hkv;
   const int rest = unit / p.Hkv;
@@ -140,7 +147,7 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
   if (row >= p.n_rows) return;
   if (p.n_chunks > 0 && row_in_chunk(p, row)) return;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lane = threadIdx.x;
   const int seq = __ldg(p.seq_ids + row);
   const int pos = __ldg(p.positions + row);
   const bool q_bf16 = p.q_is_bf16 != 0;
@@ -149,8 +156,8 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
 
   if (seq < 0 || seq >= p.num_seqs || pos < 0 || pos >= p.max_blocks * P) {
     if (split == 0) {
-      for (int i = tid; i < G * D; i += Geo::THREADS) store_out(p.out, q_bf16, out_row * D + i, 0.0f);
-      if (tid == 0) record_error(p.status, ST_OUT_OF_RANGE);
+      for (int i = lane; i < G * D; i += 32) store_out(p.out, q_bf16, out_row * D + i, 0.0f);
+      if (lane == 0) record_error(p.status, ST_OUT_OF_RANGE);
     }
     return;
   }
@@ -167,30 +174,31 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   MmaSmemHeader* hdr = reinterpret_cast<MmaSmemHeader*>(smem);
   unsigned char* ring = smem + mma_header_bytes();
-  if (tid == 0) {
+  if (lane == 0) {
     for (int s = 0; s < NST; ++s) mbar_init(&hdr->full[s], 1);
     mbar_init(&hdr->stall, 1);
     hdr->bad = 0;
     hdr->last = 0;
     fence_barrier_init();
   }
+  bool unit_bad;
   {
+    // the unit's page ids, range-checked before any copy
     const int32_t* bt = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + j0;
     bool bad = false;
-    for (int i = tid; i < npg && i < kMaxUnitPages; i += Geo::THREADS) {
+    for (int i = lane; i < npg && i < kMaxUnitPages; i += 32) {
       const int pid = __ldg(bt + i);
       bad |= pid < 0 || pid >= p.num_pages;
       hdr->pid[i] = pid;
     }
-    sync_threads_n<Geo::THREADS>();
-    if (bad) {
+    unit_bad = __any_sync(0xffffffffu, bad);
+    __syncwarp();  // page ids and barrier init visible to lane 0
+    if (unit_bad && lane == 0) {
       hdr->bad = 1;
       record_error(p.status, ST_OUT_OF_RANGE);
     }
   }
-  sync_threads_n<Geo::THREADS>();
-  const bool unit_bad = hdr->bad != 0;
-  if (tid == 0 && !unit_bad) {
+  if (lane == 0 && !unit_bad) {
     const int first = min(NST, nstage);
     for (int n = 0; n < first; ++n) mma_issue_stage(p, hdr, ring, n, n, t_begin, t_end, j0, h, lg_p);
   }
@@ -238,15 +246,19 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
     }
   }
 
-  // ---- per-warp state: heads 2 t4 and 2 t4 + 1; O^T rows d(i, g4) = 16 g4 + i and
-  // d(i, g4 + 8) = 16 g4 + 8 + i for m-tile i
-  float m_ref[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
-  float o[8][4];
+  // ---- softmax state: heads 2 t4 and 2 t4 + 1; O^T rows d(i, g4) = 16 g4 + i and
+  // d(i, g4 + 8) = 16 g4 + 8 + i for m-tile i.  The sums of the weights come
+  // from one more MMA per 16 keys with an all-ones A: lsum[0] / lsum[1] hold
+  // heads 2 t4 / 2 t4 + 1 (lsum[2..3] repeat them), summed from the same
+  // f16-rounded weights that meet V.
+  float m_ref[2] = {-INFINITY, -INFINITY};
+  float o[8][4], lsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+  const uint32_t ones[4] = {0x3c003c00u, 0x3c003c00u, 0x3c003c00u, 0x3c003c00u};  // f16x2 (1, 1)
 
   int drain_n = -1;  // the stage a wait gave up on
-  for (int n = warp; n < nstage && !unit_bad; n += NW) {
+  for (int n = 0; n < nstage && !unit_bad; ++n) {
     const int s = n % NST;
     bool got = mbar_wait(&hdr->full[s], (n / NST) & 1, p.wait_limit);
     if (p.debug_stall) got = got && mbar_wait(&hdr->stall, 0, p.wait_limit);  // runs out by construction
@@ -261,11 +273,14 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
     unsigned char* ks = ring + static_cast<size_t>(s) * kMmaStageBytes;
     unsigned char* vs = ks + ST * 128;
     const int n_valid = min(ST, t_end - (t_begin + n * ST));  // 1..32
-    // ---- S^T = K . Q^T for the stage's two 16-key m-tiles
+    const bool full = n_valid == ST;
+    // ---- S^T = K . Q^T for the stage's two 16-key m-tiles; the two k halves
+    // of each head block accumulate separately (shorter dependency chains)
+    // and are added at the end
     float sc[2][4];
 #pragma unroll
     for (int mi = 0; mi < 2; ++mi) {
-      sc[mi][0] = sc[mi][1] = sc[mi][2] = sc[mi][3] = 0.0f;
+      float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       const int r = 16 * mi + (lane & 7) + ((lane >> 3) & 1) * 8;  // row this lane addresses for ldmatrix
 #pragma unroll
       for (int kb = 0; kb < 4; ++kb) {
@@ -275,58 +290,66 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
                                 e4m3x2_to_f16x2(kr[2], true), e4m3x2_to_f16x2(kr[3], true)};
         const uint32_t a1[4] = {e4m3x2_to_f16x2(kr[0], false), e4m3x2_to_f16x2(kr[1], false),
                                 e4m3x2_to_f16x2(kr[2], false), e4m3x2_to_f16x2(kr[3], false)};
-        mma_f16_16816(sc[mi], a0, qf[kb][0], qf[kb][1]);
-        mma_f16_16816(sc[mi], a1, qf[kb][2], qf[kb][3]);
+        mma_f16_16816(sa, a0, qf[kb][0], qf[kb][1]);
+        mma_f16_16816(sb, a1, qf[kb][2], qf[kb][3]);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int key = 16 * mi + g4 + (c >> 1) * 8;
+        sc[mi][c] = (full || key < n_valid) ? __fadd_rn(sa[c], sb[c]) : -INFINITY;
       }
     }
-    // ---- online softmax: this lane holds keys 16 mi + g4 (+8) for heads 2 t4 (+1)
-    const bool full = n_valid == ST;
+    // ---- online softmax (log2 domain): this lane holds keys 16 mi + g4 (+8)
+    // for heads 2 t4 (+1).  t = score * scale - reference; the reference of a
+    // head moves only when some weight would exceed 2^kRescaleSlack, which a
+    // single vote detects, so the common stage needs no max reduction.
+    float t[2][4];
+    float tmax = -INFINITY;
 #pragma unroll
     for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int key = 16 * mi + g4 + (c >> 1) * 8;
-        sc[mi][c] = (full || key < n_valid) ? __fmul_rn(sc[mi][c], score_scale) : -INFINITY;
+        t[mi][c] = fmaf(sc[mi][c], score_scale, -m_ref[c & 1]);
+        tmax = fmaxf(tmax, t[mi][c]);
       }
-    uint32_t pb[2][2];  // P^T fragments: [k-step][keys 0..7 / 8..15 of it]
-    float alpha2[2];
-    bool rescale = false;
+    if (__any_sync(0xffffffffu, tmax > kRescaleSlack)) {
+      float alpha[2];
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      float mx = fmaxf(fmaxf(sc[0][hh], sc[0][2 + hh]), fmaxf(sc[1][hh], sc[1][2 + hh]));
+      for (int hh = 0; hh < 2; ++hh) {
+        float mx = fmaxf(fmaxf(__fmul_rn(sc[0][hh], score_scale), __fmul_rn(sc[0][2 + hh], score_scale)),
+                         fmaxf(__fmul_rn(sc[1][hh], score_scale), __fmul_rn(sc[1][2 + hh], score_scale)));
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      alpha2[hh] = 1.0f;
-      if (mx > __fadd_rn(m_ref[hh], kRescaleSlack)) {
-        alpha2[hh] = ex2(__fsub_rn(m_ref[hh], mx));
-        rescale = true;
-        m_ref[hh] = mx;
-        l_run[hh] = __fmul_rn(l_run[hh], alpha2[hh]);
+        for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        alpha[hh] = 1.0f;
+        if (mx > __fadd_rn(m_ref[hh], kRescaleSlack)) {
+          alpha[hh] = ex2(__fsub_rn(m_ref[hh], mx));  // 0 on the first stage
+          m_ref[hh] = mx;
+        }
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        o[i][0] = __fmul_rn(o[i][0], alpha[0]);
+        o[i][1] = __fmul_rn(o[i][1], alpha[1]);
+        o[i][2] = __fmul_rn(o[i][2], alpha[0]);
+        o[i][3] = __fmul_rn(o[i][3], alpha[1]);
+      }
+      lsum[0] = __fmul_rn(lsum[0], alpha[0]);
+      lsum[1] = __fmul_rn(lsum[1], alpha[1]);
+      lsum[2] = __fmul_rn(lsum[2], alpha[0]);
+      lsum[3] = __fmul_rn(lsum[3], alpha[1]);
 #pragma unroll
       for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const float v = sc[mi][2 * c2 + hh];
-          const float w = v == -INFINITY ? 0.0f : ex2(__fsub_rn(v, m_ref[hh]));
-          sc[mi][2 * c2 + hh] = w;
-          l_run[hh] = __fadd_rn(l_run[hh], w);
-        }
+        for (int c = 0; c < 4; ++c) t[mi][c] = fmaf(sc[mi][c], score_scale, -m_ref[c & 1]);
     }
-    if (__any_sync(0xffffffffu, rescale)) {  // rare: the reference maximum moved
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        o[i][0] = __fmul_rn(o[i][0], alpha2[0]);
-        o[i][1] = __fmul_rn(o[i][1], alpha2[1]);
-        o[i][2] = __fmul_rn(o[i][2], alpha2[0]);
-        o[i][3] = __fmul_rn(o[i][3], alpha2[1]);
-      }
-    }
+    // weights (masked keys: 2^-inf = 0), to f16 and into B-fragment order:
+    // C layout (key g4 / g4+8, heads 2t4, 2t4+1) -> B layout (head g4, keys 2t4, 2t4+1)
+    uint32_t pb[2][2];  // P^T fragments: [k-step][keys 0..7 / 8..15 of it]
 #pragma unroll
     for (int mi = 0; mi < 2; ++mi) {
-      // C layout (key g4 / g4+8, heads 2t4, 2t4+1) -> B layout (head g4, keys 2t4, 2t4+1)
-      pb[mi][0] = movmatrix_trans(pack_f16x2(sc[mi][0], sc[mi][1]));
-      pb[mi][1] = movmatrix_trans(pack_f16x2(sc[mi][2], sc[mi][3]));
+      pb[mi][0] = movmatrix_trans(pack_f16x2(ex2(t[mi][0]), ex2(t[mi][1])));
+      pb[mi][1] = movmatrix_trans(pack_f16x2(ex2(t[mi][2]), ex2(t[mi][3])));
+      mma_f16_16816(lsum, ones, pb[mi][0], pb[mi][1]);
     }
     // ---- value rows past the row's position: zero them before they meet weight 0
     if (!full) {
@@ -366,73 +389,91 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
         mma_f16_16816(o[4 * w + 3], a_j3, pb[mi][0], pb[mi][1]);
       }
     }
-    // ---- release: this warp was the slot's only reader; refill it
+    // ---- release the slot and refill it
     __syncwarp();
     if (lane == 0 && n + NST < nstage) {
       fence_proxy_async();
       mma_issue_stage(p, hdr, ring, n + NST, s, t_begin, t_end, j0, h, lg_p);
     }
   }
-  // After a wait gave up on stage n, stages n and n + 4 (if any) may still be
-  // in flight into this warp's slots: let them land before the ring is reused.
+  // After a wait gave up on stage n, stages n .. n + NST - 1 may still be in
+  // flight: let them land before the ring is reused.
   if (drain_n >= 0 && lane == 0) {
-    mbar_wait(&hdr->full[drain_n % NST], (drain_n / NST) & 1, kDrainWaitLimit);
-    const int n2 = drain_n + NW;
-    if (n2 < nstage) mbar_wait(&hdr->full[n2 % NST], (n2 / NST) & 1, kDrainWaitLimit);
+    for (int m = drain_n; m < min(drain_n + NST, nstage); ++m)
+      mbar_wait(&hdr->full[m % NST], (m / NST) & 1, kDrainWaitLimit);
   }
-  // complete each head's sum over the lanes that hold its other keys
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) l_run[hh] = __fadd_rn(l_run[hh], __shfl_xor_sync(0xffffffffu, l_run[hh], off));
+  __syncwarp();
+  const bool bad = hdr->bad != 0;
 
-  sync_threads_n<Geo::THREADS>();
+  if (nsplit == 1) {
+    // ---- straight from the fragments: out = o * (v_scale / l), 16 bytes a store
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int head = 2 * t4 + hh;
+      if (head < G) {
+        const float r = __fdiv_rn(p.v_scale, lsum[hh]);
+        uint32_t w0[4], w1[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // a unit that hit an error writes zeros
+          w0[i] = bad ? 0u : pack_bf16x2(__fmul_rn(o[2 * i][hh], r), __fmul_rn(o[2 * i + 1][hh], r));
+          w1[i] = bad ? 0u : pack_bf16x2(__fmul_rn(o[2 * i][2 + hh], r), __fmul_rn(o[2 * i + 1][2 + hh], r));
+        }
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + (out_row + head) * D + 16 * g4);
+        dst[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+        dst[1] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+      }
+    }
+    return;
+  }
 
-  // ---- the 4 warps' states to shared memory in the SIMT unit's layout, then
-  // the same fixed-order merges and epilogue
-  float* red_acc = reinterpret_cast<float*>(ring);  // [NW][G][D]
-  float* red_ml = red_acc + NW * G * D;             // [NW][G][2]
+  // ---- split row: the state to shared memory in the SIMT unit's layout (one
+  // warp), then the same partial publication and split merge
+  float* red_acc = reinterpret_cast<float*>(ring);  // [G][D]
+  float* red_ml = red_acc + G * D;                  // [G][2]
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     const int head = 2 * t4 + hh;
     if (head < G) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        red_acc[(warp * G + head) * D + 16 * g4 + i] = o[i][hh];
-        red_acc[(warp * G + head) * D + 16 * g4 + 8 + i] = o[i][2 + hh];
+        red_acc[head * D + 16 * g4 + i] = o[i][hh];
+        red_acc[head * D + 16 * g4 + 8 + i] = o[i][2 + hh];
       }
       if (g4 == 0) {
-        red_ml[(warp * G + head) * 2] = m_ref[hh];
-        red_ml[(warp * G + head) * 2 + 1] = l_run[hh];
+        red_ml[head * 2] = m_ref[hh];
+        red_ml[head * 2 + 1] = lsum[hh];
       }
     }
   }
-  sync_threads_n<Geo::THREADS>();
-  decode_finish<D, G, KV_E4M3, NW, Geo::THREADS>(p, hdr->bad != 0, &hdr->last, red_acc, red_ml, out_row, row, h,
-                                               split, nsplit, q_bf16, NST * kMmaStageBytes);
+  __syncwarp();
+  decode_finish<D, G, KV_E4M3, 1, 32>(p, bad, &hdr->last, red_acc, red_ml, out_row, row, h, split, nsplit, q_bf16,
+                                      NST * kMmaStageBytes);
 }
 
-template <int G>
-__global__ void __launch_bounds__(MmaGeom<G>::THREADS, MmaGeom<G>::MIN_CTAS) decode_mma_kernel(const __grid_constant__ AttnParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];  // aligned to 1024 by hand below
-  decode_unit_mma<G>(p, static_cast<int>(blockIdx.x), smem);
+template <int G, int NST>
+__global__ void __launch_bounds__(32) decode_mma_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];  // aligned to 1024 by hand in the unit
+  decode_unit_mma<G, NST>(p, static_cast<int>(blockIdx.x), smem);
 }
 
-constexpr size_t mma_smem_bytes() { return 1024 + mma_header_bytes() + MmaGeom<1>::STAGES * kMmaStageBytes; }
+#ifndef PA_MMA_STAGES
+#define PA_MMA_STAGES 2
+#endif
+constexpr int kMmaStages = PA_MMA_STAGES;  // ring slots per one-warp CTA (measured: fewer slots, more resident units, faster)
 
 template <int G>
 cudaError_t launch_decode_mma_inst(const AttnParams& p, cudaStream_t stream) {
-  const size_t smem = mma_smem_bytes();
-  static int attr_bytes = 0;
-  if (static_cast<int>(smem) > attr_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  using Geo = MmaGeom<G, kMmaStages>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G, kMmaStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Geo::SMEM));
     if (e != cudaSuccess) return e;
-    attr_bytes = static_cast<int>(smem);
+    attr_set = true;
   }
   const long long units = static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
   if (units <= 0) return cudaSuccess;
-  decode_mma_kernel<G><<<static_cast<unsigned>(units), MmaGeom<G>::THREADS, smem, stream>>>(p);
+  decode_mma_kernel<G, kMmaStages><<<static_cast<unsigned>(units), Geo::THREADS, Geo::SMEM, stream>>>(p);
   count_launch();
   return cudaGetLastError();
 }

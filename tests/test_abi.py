@@ -82,6 +82,9 @@ def test_host_side_errors_launch_nothing(lib):
         assert att(hq=18) == pa.PA_ERR_UNSUPPORTED         # group of 9
         assert att(qd=pa.PA_FP8_E4M3) == pa.PA_ERR_INVALID_ARG
         assert att(out=None) == pa.PA_ERR_INVALID_ARG
+        assert att(out=vp(0x100008)) == pa.PA_ERR_INVALID_ARG   # out not 16-byte aligned
+        assert lib.pa_attention(h, 4, vp(0x100002), pa.PA_BF16, 8, dev, dev, dev, 4, 4, None, 0, 0.0, dev, None, 0,
+                                None, None) == pa.PA_ERR_INVALID_ARG  # q not 16-byte aligned
         assert att(n=0, out=None) == pa.PA_OK
         two = (pa.Chunk * 2)(pa.Chunk(0, 3), pa.Chunk(2, 2))
         assert att(chunks=two, nc=2) == pa.PA_ERR_INVALID_ARG   # overlapping chunks
