@@ -136,7 +136,8 @@ size_t pa_attention_workspace_bytes(const pa_pool *pool, int32_t n_rows, int32_t
  *   softmax_scale <= 0 selects 1 / sqrt(head_dim)
  *   workspace    device memory of at least pa_attention_workspace_bytes(...), 256-byte
  *                aligned, ZERO-FILLED BEFORE ITS FIRST USE; every call leaves it
- *                zero-filled again, so it is reused without clearing.  Calls that share a
+ *                zero-filled again, so it is reused without clearing (except after a call
+ *                that reported PA_ERR_TIMEOUT: clear it again).  Calls that share a
  *                workspace must not overlap on the GPU.  May be NULL when 0 bytes are needed.
  * Each row attends keys 0..positions[r] of its own sequence (its own token
  * included, so append the step's rows first).  A row's output bits depend only

@@ -388,16 +388,19 @@ pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dt
   }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
+  cudaError_t e = cudaErrorNotSupported;
   if (p.n_prefill_ctas > 0) {
     e = pa::launch_mixed_bf16(p, s);
-  } else if (mma_decode) {
-    e = pa::launch_decode_e4m3_mma(p, s);
   } else {
-    switch (d.kv_dtype) {
-      case PA_F32: e = pa::launch_decode_f32(p, s); break;
-      case PA_BF16: e = pa::launch_decode_bf16(p, s); break;
-      default: e = pa::launch_decode_e4m3(p, s); break;
+    // the tensor-core units decline a grid beyond their limits (more than
+    // 65535 splits a row): the SIMT units take it
+    if (mma_decode) e = pa::launch_decode_e4m3_mma(p, s);
+    if (e == cudaErrorNotSupported) {
+      switch (d.kv_dtype) {
+        case PA_F32: e = pa::launch_decode_f32(p, s); break;
+        case PA_BF16: e = pa::launch_decode_bf16(p, s); break;
+        default: e = pa::launch_decode_e4m3(p, s); break;
+      }
     }
   }
   if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "no decode kernel for head_dim %d, group %d", d.head_dim, G);

@@ -15,7 +15,8 @@
 //     context lengths of a 7B-class decode batch), so many small CTAs per SM
 //     keep more units' copies in flight than a few wide ones, and no
 //     cross-warp merge is needed.  The warp waits on, consumes and refills
-//     its ring of NST slots in stage order.
+//     its ring of NST slots in stage order; NST (2, 4 or 8) follows the
+//     number of units in the launch.
 //   * Stages of 32 tokens arrive by 2-D tensor-map copies (box: 128 bytes x
 //     min(P, 32) rows of one page of one kv head) into 128-byte swizzled
 //     shared-memory tiles, so that ldmatrix and 16-byte row loads are free of
@@ -148,11 +149,26 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
   if (p.n_chunks > 0 && row_in_chunk(p, row)) return;
 
   const int lane = threadIdx.x;
+  const int g4 = lane >> 2;  // fragment group: key row (QK), head element block (PV), query head (B operand)
+  const int t4 = lane & 3;   // thread in group
+  const size_t out_row = static_cast<size_t>(row) * p.Hq + static_cast<size_t>(h) * G;
+  // The query words this lane needs (bf16), loaded first so that their latency
+  // overlaps the sequence and page-id lookups: head g4 of the group (head 0
+  // stands in for heads >= G), elements 32kb + 4 t4 .. +3 and 32kb + 16 + 4 t4 .. +3.
+  uint2 qraw[4][2];
+  {
+    const uint2* qs = reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.q) +
+                                                     (out_row + (g4 < G ? g4 : 0)) * D);
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+      qraw[kb][0] = __ldg(qs + 8 * kb + t4);
+      qraw[kb][1] = __ldg(qs + 8 * kb + 4 + t4);
+    }
+  }
   const int seq = __ldg(p.seq_ids + row);
   const int pos = __ldg(p.positions + row);
-  const bool q_bf16 = p.q_is_bf16 != 0;
+  const bool q_bf16 = p.q_is_bf16 != 0;  // always true here: the tensor-core units take bf16 queries
   const int P = p.P;
-  const size_t out_row = static_cast<size_t>(row) * p.Hq + static_cast<size_t>(h) * G;
 
   if (seq < 0 || seq >= p.num_seqs || pos < 0 || pos >= p.max_blocks * P) {
     if (split == 0) {
@@ -203,9 +219,6 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
     for (int n = 0; n < first; ++n) mma_issue_stage(p, hdr, ring, n, n, t_begin, t_end, j0, h, lg_p);
   }
 
-  const int g4 = lane >> 2;  // fragment group: key row (QK), head element block (PV), query head (B operand)
-  const int t4 = lane & 3;   // thread in group
-
   // ---- query fragments (B of Q.K), f16, in the permuted k order of the K fragments:
   // for head block kb (32 elements) the first MMA reads elements 32kb + 4 t4 + {0,1}
   // and 32kb + 16 + 4 t4 + {0,1}, the second + 2.  Head g4 of the group (zero if >= G).
@@ -215,18 +228,16 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
     float qv[4][8];
     float amax = 0.0f;
     const bool head_ok = g4 < G;
-    const size_t qoff = (out_row + (head_ok ? g4 : 0)) * D;
 #pragma unroll
     for (int kb = 0; kb < 4; ++kb) {
-      float f[4];
-      load_q_vec<4>(p.q, q_bf16, qoff + 32 * kb + 4 * t4, f);
+      const uint2 w0 = qraw[kb][0], w1 = qraw[kb][1];
+      const float f[8] = {bf16lo(w0.x), bf16hi(w0.x), bf16lo(w0.y), bf16hi(w0.y),
+                          bf16lo(w1.x), bf16hi(w1.x), bf16lo(w1.y), bf16hi(w1.y)};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) qv[kb][i] = head_ok ? f[i] : 0.0f;
-      load_q_vec<4>(p.q, q_bf16, qoff + 32 * kb + 16 + 4 * t4, f);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) qv[kb][4 + i] = head_ok ? f[i] : 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(qv[kb][i]));
+      for (int i = 0; i < 8; ++i) {
+        qv[kb][i] = head_ok ? f[i] : 0.0f;
+        amax = fmaxf(amax, fabsf(qv[kb][i]));
+      }
     }
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -451,31 +462,58 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
 }
 
 template <int G, int NST>
-__global__ void __launch_bounds__(32) decode_mma_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(32, 8) decode_mma_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(128) unsigned char smem[];  // aligned to 1024 by hand in the unit
   decode_unit_mma<G, NST>(p, static_cast<int>(blockIdx.x), smem);
 }
 
-#ifndef PA_MMA_STAGES
-#define PA_MMA_STAGES 2
-#endif
-constexpr int kMmaStages = PA_MMA_STAGES;  // ring slots per one-warp CTA (measured: fewer slots, more resident units, faster)
-
-template <int G>
-cudaError_t launch_decode_mma_inst(const AttnParams& p, cudaStream_t stream) {
-  using Geo = MmaGeom<G, kMmaStages>;
+template <int G, int NST>
+cudaError_t launch_decode_mma_nst(const AttnParams& p, cudaStream_t stream, unsigned units) {
+  using Geo = MmaGeom<G, NST>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G, kMmaStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Geo::SMEM));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const long long units = static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
-  if (units <= 0) return cudaSuccess;
-  decode_mma_kernel<G, kMmaStages><<<static_cast<unsigned>(units), Geo::THREADS, Geo::SMEM, stream>>>(p);
+  decode_mma_kernel<G, NST><<<units, Geo::THREADS, Geo::SMEM, stream>>>(p);
   count_launch();
   return cudaGetLastError();
+}
+
+// Units resident on the GPU at once with an NST-slot ring (from the shared
+// memory each one-warp CTA takes), queried once.
+template <int G, int NST>
+long long mma_resident_units() {
+  static long long cap = -1;
+  if (cap < 0) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_mma_kernel<G, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(MmaGeom<G, NST>::SMEM)) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<G, NST>, 32, MmaGeom<G, NST>::SMEM) !=
+            cudaSuccess)
+      return 0;
+    cap = static_cast<long long>(sms) * per_sm;
+  }
+  return cap;
+}
+
+// The ring depth follows the number of units: many short units want many
+// resident CTAs (two slots each); few long ones want each CTA to keep more
+// copies in flight.  Take the deepest ring whose CTAs all fit on the GPU at
+// once, else two slots.  The depth changes no arithmetic: a row's output bits
+// do not depend on it.
+template <int G>
+cudaError_t launch_decode_mma_inst(const AttnParams& p, cudaStream_t stream) {
+  const long long units = static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
+  if (units <= 0) return cudaSuccess;
+  if (units > 0x7fffffffLL) return cudaErrorNotSupported;
+  const unsigned u = static_cast<unsigned>(units);
+  if (units <= mma_resident_units<G, 8>()) return launch_decode_mma_nst<G, 8>(p, stream, u);
+  if (units <= mma_resident_units<G, 4>()) return launch_decode_mma_nst<G, 4>(p, stream, u);
+  return launch_decode_mma_nst<G, 2>(p, stream, u);
 }
 
 }  // namespace pa

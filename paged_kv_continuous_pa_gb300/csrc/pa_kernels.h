@@ -12,7 +12,10 @@ constexpr int kMaxChunks = 16;          // prefill chunks per pa_attention call
 constexpr int kDefaultSplitTokens = 4096;
 constexpr uint32_t kDefaultWaitLimit = 1000000;  // microseconds one bounded wait may take (one second)
 constexpr uint32_t kDrainWaitLimit = 1000000;    // microseconds spent draining copies on an error path
-constexpr uint32_t kWaitHintNs = 10000;          // longest sleep inside one mbarrier poll
+#ifndef PA_WAIT_HINT_NS
+#define PA_WAIT_HINT_NS 10000
+#endif
+constexpr uint32_t kWaitHintNs = PA_WAIT_HINT_NS;  // longest sleep inside one mbarrier poll (0: poll without a hint)
 constexpr int kMaxStages = 16;          // decode pipeline depth upper bound
 constexpr int kDecodeWarps = 4;         // warps of a decode CTA
 constexpr int kStageTokens = 32;        // tokens per decode pipeline stage
