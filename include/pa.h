@@ -153,6 +153,27 @@ pa_status pa_attention(const pa_pool *pool, int32_t n_rows, const void *q, pa_dt
                        const pa_chunk *chunks, int32_t n_chunks, float softmax_scale, void *out,
                        void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream);
 
+/* One decode/prefill step: pa_append_kv of the step's rows, then pa_attention
+ * over the same rows, as two launches on `stream` in which the attention kernel
+ * is a programmatic dependent of the append: its CTAs start (query, sequence
+ * and page-id lookups) while the append runs and wait for the append's
+ * completion before their first read of the pools.  Between the two launches
+ * of a step the pages put the launch gap of eager decoding ("Building an LLM
+ * runtime from scratch on NVIDIA H100", section "Bug #2: Eager Decode and the
+ * CUDA Graph Necessity"; "GPU inference engine engineering", section "Speed
+ * that counts end to end"); this removes the attention's start-up latency from
+ * the step, and the pair stays capturable in a CUDA graph.
+ *   k_new, v_new, kv_in_dtype: as pa_append_kv's k_new, v_new, in_dtype
+ *   the other arguments: as pa_attention
+ * Results are bit-identical to pa_append_kv followed by pa_attention on the
+ * same stream.  Every argument of both is checked before anything is
+ * launched; errors as for those two calls. */
+pa_status pa_step(const pa_pool *pool, int32_t n_rows, const void *q, pa_dtype q_dtype, int32_t num_q_heads,
+                  const void *k_new, const void *v_new, pa_dtype kv_in_dtype, const int32_t *seq_ids,
+                  const int32_t *positions, const int32_t *block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                  const pa_chunk *chunks, int32_t n_chunks, float softmax_scale, void *out, void *workspace,
+                  size_t workspace_bytes, int32_t *status_dev, void *stream);
+
 /* pa_attention without a workspace argument, for callers that cannot allocate
  * device memory: code handed only its input and output buffers by a host
  * runtime that owns and budgets all device memory (a plugin interface), or a

@@ -65,6 +65,12 @@ class DeviceStep:
         pa.append_kv(self.pool, self.k_new, self.v_new, self.seq_ids, self.positions, self.block_tables,
                      status=self.status, stream=stream)
 
+    def step(self, stream=None, out=None):
+        """append_step() and attend() as one pa_step call."""
+        pa.step(self.pool, self.q, self.k_new, self.v_new, self.seq_ids, self.positions, self.block_tables,
+                self.out if out is None else out, chunks=self.wl.chunks, softmax_scale=self.wl.softmax_scale,
+                workspace=self.workspace, status=self.status, stream=stream)
+
     def attend(self, stream=None, out=None):
         pa.attention(self.pool, self.q, self.seq_ids, self.positions, self.block_tables,
                      self.out if out is None else out, chunks=self.wl.chunks, softmax_scale=self.wl.softmax_scale,

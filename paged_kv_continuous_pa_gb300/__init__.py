@@ -74,6 +74,9 @@ def load(path: str = LIB_PATH):
         L.pa_attention_noalloc.argtypes = [vp, i32, vp, i32, i32, vp, vp, vp, i32, i32, ctypes.POINTER(Chunk), i32,
                                            f32, vp, vp, vp]
         L.pa_attention_noalloc.restype = st
+        L.pa_step.argtypes = [vp, i32, vp, i32, i32, vp, vp, i32, vp, vp, vp, i32, i32, ctypes.POINTER(Chunk), i32,
+                              f32, vp, vp, sz, vp, vp]
+        L.pa_step.restype = st
         L.pa_set_split_tokens.argtypes = [i32]
         L.pa_set_split_tokens.restype = st
         L.pa_get_split_tokens.argtypes = []
@@ -205,6 +208,26 @@ def attention(pool: Pool, q, seq_ids, positions, block_tables, out,
     _check(load().pa_attention(pool.handle, n, _ptr(q), _dtype_code(q), num_q_heads, _ptr(seq_ids), _ptr(positions),
                                _ptr(block_tables), num_seqs, max_blocks, arr if chunks else None, len(chunks),
                                float(softmax_scale), _ptr(out), ws_ptr, ws_len, _ptr(status), _stream(stream)))
+
+
+def step(pool: Pool, q, k_new, v_new, seq_ids, positions, block_tables, out,
+         chunks: Sequence[Tuple[int, int]] = (), softmax_scale: float = 0.0, workspace=None, status=None, stream=None):
+    """append_kv() then attention() of the same rows as one call: the attention
+    kernel starts while the append runs (bit-identical to the two calls)."""
+    n = int(seq_ids.shape[0])
+    num_q_heads = int(q.shape[1])
+    num_seqs, max_blocks = (int(x) for x in block_tables.shape)
+    if out.dtype != q.dtype or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must match q's shape and dtype")
+    if k_new.dtype != v_new.dtype:
+        raise ValueError("k_new and v_new must share a dtype")
+    arr = (Chunk * max(1, len(chunks)))(*[Chunk(int(b), int(c)) for b, c in chunks])
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pa_step(pool.handle, n, _ptr(q), _dtype_code(q), num_q_heads, _ptr(k_new), _ptr(v_new),
+                          _dtype_code(k_new), _ptr(seq_ids), _ptr(positions), _ptr(block_tables), num_seqs, max_blocks,
+                          arr if chunks else None, len(chunks), float(softmax_scale), _ptr(out), ws_ptr, ws_len,
+                          _ptr(status), _stream(stream)))
 
 
 def attention_noalloc(pool: Pool, q, seq_ids, positions, block_tables, out,

@@ -193,40 +193,18 @@ void pa::set_last_error(const char* fmt, ...) {
   va_end(ap);
 }
 
-extern "C" {
+namespace {
 
-size_t pa_pool_bytes(const pa_pool_desc* desc) {
-  if (check_desc(desc) != PA_OK) return 0;
-  return static_cast<size_t>(desc->num_pages) * desc->num_kv_heads * desc->page_size * desc->head_dim *
-         elt_bytes(desc->kv_dtype);
-}
-
-pa_status pa_pool_create(const pa_pool_desc* desc, void* k_pool, void* v_pool, pa_pool** out) {
-  if (out == nullptr) return fail(PA_ERR_INVALID_ARG, "out is NULL");
-  *out = nullptr;
-  pa_status st = check_desc(desc);
-  if (st != PA_OK) return st;
-  if (k_pool == nullptr || v_pool == nullptr) return fail(PA_ERR_INVALID_ARG, "pool buffers must not be NULL");
-  if (!aligned(k_pool, 16) || !aligned(v_pool, 16)) return fail(PA_ERR_INVALID_ARG, "pool buffers must be 16-byte aligned");
-  pa_pool* p = new (std::nothrow) pa_pool;
-  if (p == nullptr) return fail(PA_ERR_INVALID_ARG, "out of host memory");
-  p->desc = *desc;
-  if (p->desc.kv_dtype != PA_FP8_E4M3) p->desc.k_scale = p->desc.v_scale = 1.0f;
-  p->k = k_pool;
-  p->v = v_pool;
-  p->maps_ready = false;
-  *out = p;
-  return PA_OK;
-}
-
-void pa_pool_destroy(pa_pool* pool) { delete pool; }
-
-pa_status pa_append_kv(const pa_pool* pool, int32_t n_rows, const void* k_new, const void* v_new, pa_dtype in_dtype,
+// pa_append_kv's argument checks and launch parameters; *empty when there is nothing to do.
+pa_status build_append(const pa_pool* pool, int32_t n_rows, const void* k_new, const void* v_new, pa_dtype in_dtype,
                        const int32_t* seq_ids, const int32_t* positions, const int32_t* block_tables,
-                       int32_t num_seqs, int32_t max_blocks_per_seq, int32_t* status_dev, void* stream) {
+                       int32_t num_seqs, int32_t max_blocks_per_seq, int32_t* status_dev, pa::AppendParams* out,
+                       bool* empty) {
+  *empty = true;
   if (pool == nullptr) return fail(PA_ERR_INVALID_ARG, "pool is NULL");
   if (n_rows < 0) return fail(PA_ERR_INVALID_ARG, "n_rows %d < 0", n_rows);
   if (n_rows == 0) return PA_OK;
+  *empty = false;
   if (in_dtype != PA_F32 && in_dtype != PA_BF16)
     return fail(PA_ERR_INVALID_ARG, "append input dtype must be f32 or bf16");
   if (!k_new || !v_new || !seq_ids || !positions || !block_tables)
@@ -254,27 +232,20 @@ pa_status pa_append_kv(const pa_pool* pool, int32_t n_rows, const void* k_new, c
   p.k_scale = pool->desc.k_scale;
   p.v_scale = pool->desc.v_scale;
   p.status = status_dev;
-  cudaError_t e = pa::launch_append(p, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  *out = p;
   return PA_OK;
 }
 
-size_t pa_attention_workspace_bytes(const pa_pool* pool, int32_t n_rows, int32_t num_q_heads,
-                                    int32_t max_blocks_per_seq, const pa_chunk* chunks, int32_t n_chunks) {
-  if (pool == nullptr || n_rows <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 ||
-      num_q_heads % pool->desc.num_kv_heads != 0 || n_chunks < 0)
-    return 0;
-  // chunks of a bf16 pool may take the tile path (with bf16 queries): size for it
-  return make_plan(pool->desc, n_rows, num_q_heads, max_blocks_per_seq, chunks, n_chunks,
-                   pool->desc.kv_dtype == PA_BF16)
-      .total;
-}
-
-pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dtype q_dtype, int32_t num_q_heads,
-                       const int32_t* seq_ids, const int32_t* positions, const int32_t* block_tables,
-                       int32_t num_seqs, int32_t max_blocks_per_seq, const pa_chunk* chunks, int32_t n_chunks,
-                       float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
-                       int32_t* status_dev, void* stream) {
+// pa_attention; with `pre` (pa_step), the append `pre` describes is launched
+// once every attention argument has passed its checks, and the attention
+// kernel follows it as a programmatic dependent: its CTAs start their
+// query, sequence and page-id lookups while the append runs, and wait for it
+// before the first pool read.
+pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_dtype q_dtype, int32_t num_q_heads,
+                         const int32_t* seq_ids, const int32_t* positions, const int32_t* block_tables,
+                         int32_t num_seqs, int32_t max_blocks_per_seq, const pa_chunk* chunks, int32_t n_chunks,
+                         float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
+                         int32_t* status_dev, void* stream, const pa::AppendParams* pre) {
   if (pool == nullptr) return fail(PA_ERR_INVALID_ARG, "pool is NULL");
   const pa_pool_desc& d = pool->desc;
   if (n_rows < 0) return fail(PA_ERR_INVALID_ARG, "n_rows %d < 0", n_rows);
@@ -299,7 +270,11 @@ pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dt
           chunks[c2].row_begin < chunks[c].row_begin + chunks[c].n_rows)
         return fail(PA_ERR_INVALID_ARG, "chunks %d and %d overlap", c2, c);
   }
-  if (n_rows == 0) return PA_OK;
+  if (n_rows == 0) {
+    if (pre == nullptr) return PA_OK;
+    const cudaError_t e = pa::launch_append(*pre, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "append launch");
+  }
   if (!q || !seq_ids || !positions || !block_tables || !out)
     return fail(PA_ERR_INVALID_ARG, "attention: a device pointer is NULL");
   if (!aligned(q, 16) || !aligned(out, 16)) return fail(PA_ERR_INVALID_ARG, "q / out must be 16-byte aligned");
@@ -388,6 +363,11 @@ pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dt
   }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pre != nullptr) {
+    const cudaError_t ea = pa::launch_append(*pre, s);
+    if (ea != cudaSuccess) return cuda_fail(ea, "append launch");
+    p.dependent = 1;
+  }
   cudaError_t e = cudaErrorNotSupported;
   if (p.n_prefill_ctas > 0) {
     e = pa::launch_mixed_bf16(p, s);
@@ -406,6 +386,85 @@ pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dt
   if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "no decode kernel for head_dim %d, group %d", d.head_dim, G);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_pool_bytes(const pa_pool_desc* desc) {
+  if (check_desc(desc) != PA_OK) return 0;
+  return static_cast<size_t>(desc->num_pages) * desc->num_kv_heads * desc->page_size * desc->head_dim *
+         elt_bytes(desc->kv_dtype);
+}
+
+pa_status pa_pool_create(const pa_pool_desc* desc, void* k_pool, void* v_pool, pa_pool** out) {
+  if (out == nullptr) return fail(PA_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (k_pool == nullptr || v_pool == nullptr) return fail(PA_ERR_INVALID_ARG, "pool buffers must not be NULL");
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16)) return fail(PA_ERR_INVALID_ARG, "pool buffers must be 16-byte aligned");
+  pa_pool* p = new (std::nothrow) pa_pool;
+  if (p == nullptr) return fail(PA_ERR_INVALID_ARG, "out of host memory");
+  p->desc = *desc;
+  if (p->desc.kv_dtype != PA_FP8_E4M3) p->desc.k_scale = p->desc.v_scale = 1.0f;
+  p->k = k_pool;
+  p->v = v_pool;
+  p->maps_ready = false;
+  *out = p;
+  return PA_OK;
+}
+
+void pa_pool_destroy(pa_pool* pool) { delete pool; }
+
+pa_status pa_append_kv(const pa_pool* pool, int32_t n_rows, const void* k_new, const void* v_new, pa_dtype in_dtype,
+                       const int32_t* seq_ids, const int32_t* positions, const int32_t* block_tables,
+                       int32_t num_seqs, int32_t max_blocks_per_seq, int32_t* status_dev, void* stream) {
+  pa::AppendParams p{};
+  bool empty = true;
+  const pa_status st = build_append(pool, n_rows, k_new, v_new, in_dtype, seq_ids, positions, block_tables, num_seqs,
+                                    max_blocks_per_seq, status_dev, &p, &empty);
+  if (st != PA_OK || empty) return st;
+  cudaError_t e = pa::launch_append(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return PA_OK;
+}
+
+size_t pa_attention_workspace_bytes(const pa_pool* pool, int32_t n_rows, int32_t num_q_heads,
+                                    int32_t max_blocks_per_seq, const pa_chunk* chunks, int32_t n_chunks) {
+  if (pool == nullptr || n_rows <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 ||
+      num_q_heads % pool->desc.num_kv_heads != 0 || n_chunks < 0)
+    return 0;
+  // chunks of a bf16 pool may take the tile path (with bf16 queries): size for it
+  return make_plan(pool->desc, n_rows, num_q_heads, max_blocks_per_seq, chunks, n_chunks,
+                   pool->desc.kv_dtype == PA_BF16)
+      .total;
+}
+
+pa_status pa_attention(const pa_pool* pool, int32_t n_rows, const void* q, pa_dtype q_dtype, int32_t num_q_heads,
+                       const int32_t* seq_ids, const int32_t* positions, const int32_t* block_tables,
+                       int32_t num_seqs, int32_t max_blocks_per_seq, const pa_chunk* chunks, int32_t n_chunks,
+                       float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
+                       int32_t* status_dev, void* stream) {
+  return attention_impl(pool, n_rows, q, q_dtype, num_q_heads, seq_ids, positions, block_tables, num_seqs,
+                        max_blocks_per_seq, chunks, n_chunks, softmax_scale, out, workspace, workspace_bytes, status_dev,
+                        stream, nullptr);
+}
+
+pa_status pa_step(const pa_pool* pool, int32_t n_rows, const void* q, pa_dtype q_dtype, int32_t num_q_heads,
+                  const void* k_new, const void* v_new, pa_dtype kv_in_dtype, const int32_t* seq_ids,
+                  const int32_t* positions, const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                  const pa_chunk* chunks, int32_t n_chunks, float softmax_scale, void* out, void* workspace,
+                  size_t workspace_bytes, int32_t* status_dev, void* stream) {
+  pa::AppendParams ap{};
+  bool empty = true;
+  const pa_status st = build_append(pool, n_rows, k_new, v_new, kv_in_dtype, seq_ids, positions, block_tables,
+                                    num_seqs, max_blocks_per_seq, status_dev, &ap, &empty);
+  if (st != PA_OK) return st;
+  return attention_impl(pool, n_rows, q, q_dtype, num_q_heads, seq_ids, positions, block_tables, num_seqs,
+                        max_blocks_per_seq, chunks, n_chunks, softmax_scale, out, workspace, workspace_bytes, status_dev,
+                        stream, empty ? nullptr : &ap);
 }
 
 pa_status pa_set_split_tokens(int32_t tokens) {

@@ -16,6 +16,7 @@
 namespace pa {
 
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendParams p) {
+  griddep_launch_dependents();  // an attention launched as a dependent may start its lookups now
   const long long oct_per_row = static_cast<long long>(p.Hkv) * p.D / 8;  // octets of one K (or V) row
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long total = static_cast<long long>(p.n_rows) * 2 * oct_per_row;

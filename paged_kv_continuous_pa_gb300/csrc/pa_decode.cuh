@@ -582,6 +582,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
   sync_threads_n<Geo::THREADS>();
   const bool unit_bad = hdr->bad != 0;
   const uint64_t policy = l2_policy_evict_first();
+  griddep_wait();  // the pool rows appended by a preceding dependent-launch append are visible from here
   if (tid == 0 && !unit_bad) {
     const int first = min(NST, nstage);
     for (int n = 0; n < first; ++n) issue_stage<RB>(p, hdr, ring, n, n, t_begin, t_end, j0, h, lg_p, policy);
@@ -729,9 +730,10 @@ cudaError_t launch_decode_inst(const AttnParams& p0, cudaStream_t stream) {
   }
   const long long units = static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
   if (units <= 0) return cudaSuccess;
-  decode_kernel<D, G, KVT><<<static_cast<unsigned>(units), Geo::THREADS, smem, stream>>>(p);
+  const cudaError_t e = launch_kernel(decode_kernel<D, G, KVT>, dim3(static_cast<unsigned>(units)), dim3(Geo::THREADS),
+                                      smem, stream, p.dependent != 0, p);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 template <int KVT>

@@ -214,6 +214,7 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
       record_error(p.status, ST_OUT_OF_RANGE);
     }
   }
+  griddep_wait();  // the pool rows appended by a preceding dependent-launch append are visible from here
   if (lane == 0 && !unit_bad) {
     const int first = min(NST, nstage);
     for (int n = 0; n < first; ++n) mma_issue_stage(p, hdr, ring, n, n, t_begin, t_end, j0, h, lg_p);
@@ -477,9 +478,10 @@ cudaError_t launch_decode_mma_nst(const AttnParams& p, cudaStream_t stream, unsi
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  decode_mma_kernel<G, NST><<<units, Geo::THREADS, Geo::SMEM, stream>>>(p);
+  const cudaError_t e = launch_kernel(decode_mma_kernel<G, NST>, dim3(units), dim3(Geo::THREADS), Geo::SMEM, stream,
+                                      p.dependent != 0, p);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 // Units resident on the GPU at once with an NST-slot ring (from the shared

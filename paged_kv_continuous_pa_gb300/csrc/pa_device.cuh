@@ -121,6 +121,14 @@ __device__ __forceinline__ void sync_threads_n() {
   asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched as a dependent of the
+// previous kernel in the stream may start before that kernel finishes;
+// griddep_wait() returns once it has completed and its writes are visible
+// (at once when the kernel was launched normally).  griddep_launch_dependents()
+// lets the next kernel start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Order this thread's generic-proxy shared-memory accesses before its later
 // async-proxy (bulk-copy) operations on shared memory.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

@@ -92,12 +92,36 @@ struct AttnParams {
   float* ws_tile_ml;                      // [chunk rows][Hq][tile_splits][2] partial (max, sum)
   int32_t* ws_tile_count;                 // [tiles] finished-split counters, zero between calls
   float sm_scale_log2;                    // softmax scale * log2(e) for the tile path
+  int32_t dependent;                      // host: launch as a programmatic dependent of the append
   CUtensorMap kmap;                       // bf16 K pool as [num_pages * Hkv * P][D], box 64 x P, 128B swizzle;
                                           // e4m3 pool (D = 128): bytes [num_pages * Hkv * P][128], box 128 x min(P, 32)
   CUtensorMap vmap;                       // V pool, same geometry
 };
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+
+// Launch `kernel` normally, or (dependent) as a programmatic dependent of the
+// previous kernel in the stream: it may start while that kernel runs and must
+// call griddep_wait() before reading anything that kernel writes.
+template <typename Kernel, typename... Args>
+inline cudaError_t launch_kernel(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool dependent,
+                                 Args... args) {
+  if (!dependent) {
+    kernel<<<grid, block, smem, stream>>>(args...);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // Process-wide count of kernel launches made by the library (pa_kernel_launches).
 void count_launch();

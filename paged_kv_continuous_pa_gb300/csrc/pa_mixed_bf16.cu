@@ -42,9 +42,10 @@ cudaError_t launch_mixed_inst(const AttnParams& p0, cudaStream_t stream) {
   }
   const long long ctas = static_cast<long long>(p.n_prefill_ctas) + static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
   if (ctas <= 0) return cudaSuccess;
-  mixed_kernel<D, G><<<static_cast<unsigned>(ctas), Geo::THREADS, smem, stream>>>(p);
+  const cudaError_t e = launch_kernel(mixed_kernel<D, G>, dim3(static_cast<unsigned>(ctas)), dim3(Geo::THREADS), smem,
+                                      stream, p.dependent != 0, p);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_mixed_bf16(const AttnParams& p, cudaStream_t stream) {

@@ -195,6 +195,7 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
   constexpr uint32_t id_qk = tc::idesc_bf16_f32(kTileM, kTileN, false);
   constexpr uint32_t id_pv = tc::idesc_bf16_f32(kTileM, D, true);
   PrefillIssueLog log = {};
+  griddep_wait();  // the chunk's own rows, appended by a preceding dependent-launch append, are visible from here
   if (tid == 0 && nk > 0) {
     prefill_load_kv<D>(p, &p.kmap, Ks, &bar[BAR_K], bt, j_begin, h, fallback_pid);
     log.issue(BAR_K);

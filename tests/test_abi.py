@@ -90,6 +90,15 @@ def test_host_side_errors_launch_nothing(lib):
         assert att(chunks=two, nc=2) == pa.PA_ERR_INVALID_ARG   # overlapping chunks
         assert att(chunks=None, nc=1) == pa.PA_ERR_INVALID_ARG
         assert att(nc=17) == pa.PA_ERR_INVALID_ARG
+        # pa_step checks every argument of both halves before launching anything: a bad
+        # attention argument returns INVALID_ARG, not the CUDA error the append's launch
+        # would give on this GPU-less machine
+        stp = lambda **kw: lib.pa_step(h, 4, dev, pa.PA_BF16, kw.get("hq", 8), dev, dev, kw.get("ind", pa.PA_BF16), dev,
+                                       dev, dev, 4, 4, None, 0, 0.0, kw.get("out", dev), None, 0, None, None)
+        assert stp(ind=pa.PA_FP8_E4M3) == pa.PA_ERR_INVALID_ARG
+        assert stp(hq=5) == pa.PA_ERR_INVALID_ARG
+        assert stp(out=None) == pa.PA_ERR_INVALID_ARG
+        assert stp(out=vp(0x100008)) == pa.PA_ERR_INVALID_ARG
         # long tables need a workspace for split partials
         need = lib.pa_attention_workspace_bytes(h, 4, 8, 200, None, 0)
         assert need > 0 and need % 256 == 0
