@@ -56,7 +56,8 @@ typedef enum {
     PA_ERR_UNSUPPORTED = 2, /* host-side: a valid but unimplemented shape (e.g. head_dim 96) */
     PA_ERR_OUT_OF_RANGE = 3, /* device-side: sequence id, position or page id out of range */
     PA_ERR_TIMEOUT = 4,     /* device-side: a bounded wait on a copy gave up */
-    PA_ERR_CUDA = 5         /* a CUDA runtime call failed (launch, attribute, driver entry point) */
+    PA_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, attribute, driver entry point) */
+    PA_ERR_NO_PAGES = 6     /* host-side: an admission needs more free pages than the pool has */
 } pa_status;
 
 typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
@@ -229,6 +230,69 @@ uint64_t pa_kernel_launches(void);
 
 /* Library version string. */
 const char *pa_version(void);
+
+/* ---- Page allocator with admission (host side) ----------------------------
+ * "GPU inference engine engineering", section "Batching without running out of
+ * cache": a request is admitted only if the pages for its whole prompt AND its
+ * whole answer can be reserved up front; a refusal gives a typed reason and
+ * the numbers; the need is computable without allocating; a refused admission
+ * takes nothing.  The allocator owns page ids of one pool (0 .. num_pages-1)
+ * and the block-table rows of num_seqs sequence slots; it fills rows of a
+ * caller-owned HOST array int32 [num_seqs][max_blocks_per_seq] (unused
+ * entries -1), which the caller copies to the device for pa_append_kv /
+ * pa_attention.  Prefix sharing: a sequence may share the whole pages of an
+ * admitted parent's prompt prefix (reference counted; the page holding the
+ * prefix's last partial tokens is the sequence's own).  Page ids are handed
+ * out in a deterministic order (lowest first from a fresh allocator; a
+ * release followed by the same admission returns the same pages).  Not
+ * thread-safe: one scheduler thread owns an allocator. */
+typedef struct pa_pages pa_pages; /* opaque host object */
+
+typedef enum {
+    PA_ADMIT_OK = 0,
+    PA_ADMIT_NO_PAGES = 1,   /* fewer free pages than the admission needs (status PA_ERR_NO_PAGES) */
+    PA_ADMIT_TOO_LONG = 2,   /* prompt + answer exceed max_blocks_per_seq * page_size tokens */
+    PA_ADMIT_SEQ_IN_USE = 3, /* the sequence slot already holds pages */
+    PA_ADMIT_BAD_ARG = 4     /* slot out of range, negative counts, prefix parent not admitted */
+} pa_admit_reason;
+
+typedef struct {
+    pa_admit_reason reason;
+    int32_t pages_needed;  /* new pages the admission takes (shared prefix pages excluded) */
+    int32_t pages_free;    /* free pages when the admission was asked */
+    int32_t pages_shared;  /* whole prefix pages shared with the parent */
+    int32_t tokens;        /* prompt + answer tokens asked for */
+    int32_t max_tokens;    /* tokens one block-table row can hold */
+} pa_admit_info;
+
+/* Pages a sequence of prompt_tokens + max_new_tokens tokens needs:
+ * ceil((prompt + answer) / page_size).  No state; -1 on bad arguments.
+ * Times pa_pool_bytes(desc) / desc.num_pages it is the device memory. */
+int32_t pa_pages_needed(int32_t page_size, int32_t prompt_tokens, int32_t max_new_tokens);
+
+/* An allocator over num_pages pages of page_size tokens for num_seqs sequence
+ * slots of max_blocks_per_seq pages.  Errors: PA_ERR_INVALID_ARG. */
+pa_status pa_pages_create(int32_t num_pages, int32_t page_size, int32_t num_seqs, int32_t max_blocks_per_seq,
+                          pa_pages **out);
+void pa_pages_destroy(pa_pages *pages);
+
+/* Admit sequence slot seq for prompt_tokens + max_new_tokens tokens: reserve
+ * every page up front and write the slot's row of block_tables (host, may be
+ * NULL).  prefix_parent >= 0 shares the parent's first prefix_tokens / page_size
+ * pages (prefix_tokens <= prompt_tokens); -1 for none.  *info (may be NULL)
+ * receives the reason and the numbers.  Returns PA_OK; PA_ERR_NO_PAGES when
+ * too few pages are free; PA_ERR_INVALID_ARG for the other reasons.  A refused
+ * admission changes nothing. */
+pa_status pa_pages_admit(pa_pages *pages, int32_t seq, int32_t prompt_tokens, int32_t max_new_tokens,
+                         int32_t prefix_parent, int32_t prefix_tokens, int32_t *block_tables, pa_admit_info *info);
+
+/* Release slot seq: drop its hold on each page (a page returns to the free
+ * list when no sequence holds it) and reset its block_tables row to -1
+ * (block_tables may be NULL).  PA_ERR_INVALID_ARG if the slot holds nothing. */
+pa_status pa_pages_release(pa_pages *pages, int32_t seq, int32_t *block_tables);
+
+int32_t pa_pages_free_count(const pa_pages *pages);            /* -1 if pages is NULL */
+int32_t pa_pages_refcount(const pa_pages *pages, int32_t page); /* sequences holding page; -1 if out of range */
 
 #ifdef __cplusplus
 }

@@ -17,7 +17,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libpa_gb300.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "pa.h")
 
-PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE, PA_ERR_TIMEOUT, PA_ERR_CUDA = range(6)
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE, PA_ERR_TIMEOUT, PA_ERR_CUDA, PA_ERR_NO_PAGES = range(7)
+PA_ADMIT_OK, PA_ADMIT_NO_PAGES, PA_ADMIT_TOO_LONG, PA_ADMIT_SEQ_IN_USE, PA_ADMIT_BAD_ARG = range(5)
 PA_F32, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 
 _lib = None
@@ -38,6 +39,11 @@ class PoolDesc(ctypes.Structure):
 
 class Chunk(ctypes.Structure):
     _fields_ = [("row_begin", ctypes.c_int32), ("n_rows", ctypes.c_int32)]
+
+
+class AdmitInfo(ctypes.Structure):
+    _fields_ = [("reason", ctypes.c_int32), ("pages_needed", ctypes.c_int32), ("pages_free", ctypes.c_int32),
+                ("pages_shared", ctypes.c_int32), ("tokens", ctypes.c_int32), ("max_tokens", ctypes.c_int32)]
 
 
 def header_functions():
@@ -77,6 +83,20 @@ def load(path: str = LIB_PATH):
         L.pa_step.argtypes = [vp, i32, vp, i32, i32, vp, vp, i32, vp, vp, vp, i32, i32, ctypes.POINTER(Chunk), i32,
                               f32, vp, vp, sz, vp, vp]
         L.pa_step.restype = st
+        L.pa_pages_needed.argtypes = [i32, i32, i32]
+        L.pa_pages_needed.restype = i32
+        L.pa_pages_create.argtypes = [i32, i32, i32, i32, ctypes.POINTER(vp)]
+        L.pa_pages_create.restype = st
+        L.pa_pages_destroy.argtypes = [vp]
+        L.pa_pages_destroy.restype = None
+        L.pa_pages_admit.argtypes = [vp, i32, i32, i32, i32, i32, vp, ctypes.POINTER(AdmitInfo)]
+        L.pa_pages_admit.restype = st
+        L.pa_pages_release.argtypes = [vp, i32, vp]
+        L.pa_pages_release.restype = st
+        L.pa_pages_free_count.argtypes = [vp]
+        L.pa_pages_free_count.restype = i32
+        L.pa_pages_refcount.argtypes = [vp, i32]
+        L.pa_pages_refcount.restype = i32
         L.pa_set_split_tokens.argtypes = [i32]
         L.pa_set_split_tokens.restype = st
         L.pa_get_split_tokens.argtypes = []
@@ -173,6 +193,49 @@ class Pool:
     def __del__(self):  # pragma: no cover
         try:
             self.close()
+        except Exception:
+            pass
+
+
+def pages_needed(page_size: int, prompt_tokens: int, max_new_tokens: int) -> int:
+    """Pages a sequence of prompt + answer tokens needs (no allocation)."""
+    return int(load().pa_pages_needed(int(page_size), int(prompt_tokens), int(max_new_tokens)))
+
+
+class Pages:
+    """Host page allocator with admission over one pool's page ids; owns the host
+    block-table array int32 [num_seqs, max_blocks] (numpy) whose rows it fills."""
+
+    def __init__(self, num_pages: int, page_size: int, num_seqs: int, max_blocks: int):
+        import numpy as np
+        h = ctypes.c_void_p()
+        _check(load().pa_pages_create(int(num_pages), int(page_size), int(num_seqs), int(max_blocks), ctypes.byref(h)))
+        self.handle = h
+        self.page_size = int(page_size)
+        self.block_tables = np.full((int(num_seqs), int(max_blocks)), -1, dtype=np.int32)
+
+    def admit(self, seq: int, prompt_tokens: int, max_new_tokens: int, prefix_parent: int = -1,
+              prefix_tokens: int = 0):
+        """(status, AdmitInfo); the slot's row of block_tables is filled on PA_OK."""
+        info = AdmitInfo()
+        st = load().pa_pages_admit(self.handle, int(seq), int(prompt_tokens), int(max_new_tokens), int(prefix_parent),
+                                   int(prefix_tokens), self.block_tables.ctypes.data_as(ctypes.c_void_p),
+                                   ctypes.byref(info))
+        return int(st), info
+
+    def release(self, seq: int):
+        _check(load().pa_pages_release(self.handle, int(seq), self.block_tables.ctypes.data_as(ctypes.c_void_p)))
+
+    def free_count(self) -> int:
+        return int(load().pa_pages_free_count(self.handle))
+
+    def refcount(self, page: int) -> int:
+        return int(load().pa_pages_refcount(self.handle, int(page)))
+
+    def __del__(self):
+        try:
+            if _lib is not None and getattr(self, "handle", None):
+                _lib.pa_pages_destroy(self.handle)
         except Exception:
             pass
 

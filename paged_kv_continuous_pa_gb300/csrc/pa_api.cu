@@ -488,6 +488,7 @@ const char* pa_status_string(pa_status status) {
     case PA_ERR_OUT_OF_RANGE: return "PA_ERR_OUT_OF_RANGE";
     case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
     case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_NO_PAGES: return "PA_ERR_NO_PAGES";
   }
   return "PA_ERR_UNKNOWN";
 }

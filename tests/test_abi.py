@@ -127,5 +127,5 @@ def test_split_tokens_setting(lib):
 
 def test_status_strings(lib):
     for code, name in enumerate(["PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED", "PA_ERR_OUT_OF_RANGE",
-                                 "PA_ERR_TIMEOUT", "PA_ERR_CUDA"]):
+                                 "PA_ERR_TIMEOUT", "PA_ERR_CUDA", "PA_ERR_NO_PAGES"]):
         assert pa.status_string(code) == name
