@@ -17,7 +17,8 @@ once, plus Q and O) per launch over its CUDA-event time, against the measured
 HBM copy bandwidth.  `cpu_baseline` times the CPU oracle on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload batched_decode|mixed_step|shared_prefix|long_context|tiny_decode]
+                  [--workload batched_decode|mixed_step|shared_prefix|long_context|tiny_decode|
+                              batched_decode_fp8|long_context_fp8]
 """
 from __future__ import annotations
 
@@ -37,6 +38,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged-attention rows/s and KV-read GB/s vs GB300 HBM roofline (1 GPU)"
 L2_BYTES = 129 * 1000 * 1000  # GB300 L2
+W_CONFIG_NAMES = ("batched_decode", "mixed_step", "shared_prefix", "long_context", "tiny_decode",
+                  "batched_decode_fp8", "long_context_fp8")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -142,10 +145,8 @@ class ClockSampler:
 def make_workload(name: str, seqs: int = 0):
     import workloads as W
     if seqs > 0:
-        if name == "batched_decode":
-            return W.batched_decode(n_seqs=seqs)
-        if name == "long_context":
-            return W.long_context(n_seqs=seqs)
+        if name in ("batched_decode", "batched_decode_fp8", "long_context", "long_context_fp8"):
+            return W.CONFIGS[name](n_seqs=seqs)
         if name == "shared_prefix":
             return W.shared_prefix(n_seqs=seqs)
         raise ValueError("--seqs applies to batched_decode, long_context and shared_prefix")
@@ -411,7 +412,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="batched_decode",
-                    choices=["batched_decode", "mixed_step", "shared_prefix", "long_context", "tiny_decode"])
+                    choices=sorted(W_CONFIG_NAMES))
     ap.add_argument("--seqs", type=int, default=0, help="shrink the workload to this many sequences (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

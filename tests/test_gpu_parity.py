@@ -201,3 +201,13 @@ def test_full_mixed_step_all_rows():
 def test_full_long_context_sampled_rows():
     wl = W.long_context()
     _sampled(wl, np.array([0, 17, 40, 63]), "long context, 4 of 64 rows")
+
+
+def test_full_batched_decode_fp8_sampled_rows():
+    wl = W.batched_decode_fp8()
+    _sampled(wl, np.array([0, 1, 100, 255, 300, 511]), "batched decode fp8, 6 of 512 rows")
+
+
+def test_full_long_context_fp8_sampled_rows():
+    wl = W.long_context_fp8()
+    _sampled(wl, np.array([0, 33, 63]), "long context fp8, 3 of 64 rows")

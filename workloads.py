@@ -256,6 +256,33 @@ def long_context(seed: int = 5, n_seqs: int = 64, ctx: int = 32768) -> Workload:
                                         "D128, bf16, P16")
 
 
+def _with_fp8_scales(wl: Workload) -> Workload:
+    """Per-tensor fp8 scales: amax of every K (V) value the pools will hold, / 448, in fp32."""
+    amax_k = max(np.abs(as_f32(wl.hist_k, wl.in_dtype)).max(initial=0.0), np.abs(as_f32(wl.k_new, wl.in_dtype)).max())
+    amax_v = max(np.abs(as_f32(wl.hist_v, wl.in_dtype)).max(initial=0.0), np.abs(as_f32(wl.v_new, wl.in_dtype)).max())
+    wl.k_scale = float(np.float32(amax_k) / np.float32(448.0))
+    wl.v_scale = float(np.float32(amax_v) / np.float32(448.0))
+    return wl
+
+
+def batched_decode_fp8(seed: int = 2, n_seqs: int = 512, ctx_lo: int = 64, ctx_hi: int = 2662) -> Workload:
+    """The batched-decode shape with an fp8 e4m3 K/V cache (bf16 rows in, per-tensor scales)."""
+    rng = np.random.Generator(np.random.PCG64(seed + 100))
+    ctx = rng.integers(ctx_lo, ctx_hi + 1, size=n_seqs)
+    return _with_fp8_scales(_decode_workload(
+        "batched_decode_fp8", seed, ctx, 16, 8, 128, 32, E4M3, BF16, max_ctx=ctx_hi, spare_pages=64,
+        description=f"0.6B-class batched decode, fp8 K/V: {n_seqs} seqs ctx U[{ctx_lo},{ctx_hi}], Hq16/Hkv8, D128, "
+                    "fp8 e4m3 K/V (per-tensor scale), bf16 Q, P32, decode + append"))
+
+
+def long_context_fp8(seed: int = 5, n_seqs: int = 64, ctx: int = 32768) -> Workload:
+    """The long-context shape with an fp8 e4m3 K/V cache (bf16 rows in, per-tensor scales)."""
+    return _with_fp8_scales(_decode_workload(
+        "long_context_fp8", seed, [ctx] * n_seqs, 32, 8, 128, 16, E4M3, BF16, max_ctx=ctx, spare_pages=0,
+        description=f"long-context split-KV, fp8 K/V: {n_seqs} seqs x {ctx} tokens, Hq32/Hkv8, D128, "
+                    "fp8 e4m3 K/V (per-tensor scale), bf16 Q, P16"))
+
+
 def mixed_step(seed: int = 3, n_decode: int = 256, ctx_lo: int = 64, ctx_hi: int = 1024,
                prompt: int = 2662, chunk_at: int = 1024, chunk: int = 256) -> Workload:
     """n_decode decode rows plus one causal prefill chunk of `chunk` rows at
@@ -419,6 +446,8 @@ CONFIGS = {
     "mixed_step": mixed_step,
     "shared_prefix": shared_prefix,
     "long_context": long_context,
+    "batched_decode_fp8": batched_decode_fp8,
+    "long_context_fp8": long_context_fp8,
 }
 
 # Scaled-down versions the oracle finishes in well under a second; each still
@@ -429,4 +458,6 @@ SMALL = {
     "mixed_step": lambda: mixed_step(n_decode=16, ctx_hi=700, prompt=700, chunk_at=300, chunk=200),
     "shared_prefix": lambda: shared_prefix(n_seqs=40),
     "long_context": lambda: long_context(n_seqs=2, ctx=5000),
+    "batched_decode_fp8": lambda: batched_decode_fp8(n_seqs=24),
+    "long_context_fp8": lambda: long_context_fp8(n_seqs=2, ctx=5000),
 }
