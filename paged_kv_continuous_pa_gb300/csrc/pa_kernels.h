@@ -136,7 +136,7 @@ cudaError_t launch_decode_bf16(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_decode_e4m3(const AttnParams& p, cudaStream_t stream);
 
 // Tensor-core decode units for e4m3 pools, head_dim 128, bf16 queries,
-// 3..8 query heads per kv head; p.kmap / p.vmap must be the pools' byte views
+// 1..8 query heads per kv head; p.kmap / p.vmap must be the pools' byte views
 // [num_pages * Hkv * P][128], box 128 x min(P, 32), 128-byte swizzle.
 bool decode_e4m3_mma_eligible(int D, int G, bool q_bf16);
 cudaError_t launch_decode_e4m3_mma(const AttnParams& p, cudaStream_t stream);
