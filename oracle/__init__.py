@@ -64,6 +64,11 @@ def load(path: str):
     L.oracle_attention.argtypes = [i32, vp, i32, i32, vp, vp, vp, i32, i32, i32, i32, i32,
                                    i32, i32, f32, f32, vp, vp, f64, vp, i32]
     L.oracle_attention.restype = ctypes.c_int
+    L.oracle_append_h.argtypes = [i32, vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]
+    L.oracle_append_h.restype = ctypes.c_int
+    L.oracle_attention_h.argtypes = [i32, vp, i32, i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp,
+                                     vp, f64, vp, i32]
+    L.oracle_attention_h.restype = ctypes.c_int
     return L
 
 
@@ -115,6 +120,12 @@ def decode_pool(pool: np.ndarray, kv_dtype: int, scale: float = 1.0) -> np.ndarr
     return (table[flat.view(np.uint8)] * np.float64(scale)).reshape(pool.shape)
 
 
+def _head_scales(scale, num_kv_heads: int) -> np.ndarray:
+    """A scale per kv head as float32 (a scalar repeated)."""
+    s = np.ascontiguousarray(np.broadcast_to(np.asarray(scale, dtype=np.float32), (num_kv_heads,)))
+    return s.copy()
+
+
 def append(k_new, v_new, in_dtype, seq_ids, positions, block_tables, num_pages, page_size,
            num_kv_heads, head_dim, kv_dtype, k_scale, v_scale, k_pool, v_pool) -> int:
     """Scatter rows into the pools in place (row order).  Returns the C status (0 = ok)."""
@@ -126,6 +137,12 @@ def append(k_new, v_new, in_dtype, seq_ids, positions, block_tables, num_pages, 
     assert k_new.dtype == _NP_OF[in_dtype] and v_new.dtype == _NP_OF[in_dtype]
     assert k_pool.dtype == _NP_OF[kv_dtype] and v_pool.dtype == _NP_OF[kv_dtype]
     num_seqs, max_blocks = block_tables.shape
+    if np.ndim(k_scale) or np.ndim(v_scale):  # one scale per kv head
+        ks, vs = _head_scales(k_scale, num_kv_heads), _head_scales(v_scale, num_kv_heads)
+        return int(lib().oracle_append_h(int(seq_ids.shape[0]), _ptr(k_new), _ptr(v_new), in_dtype,
+                                         _ptr(seq_ids), _ptr(positions), _ptr(block_tables), num_seqs,
+                                         max_blocks, num_pages, page_size, num_kv_heads, head_dim,
+                                         kv_dtype, _ptr(ks), _ptr(vs), _ptr(k_pool), _ptr(v_pool)))
     return int(lib().oracle_append(int(seq_ids.shape[0]), _ptr(k_new), _ptr(v_new), in_dtype,
                                    _ptr(seq_ids), _ptr(positions), _ptr(block_tables), num_seqs,
                                    max_blocks, num_pages, page_size, num_kv_heads, head_dim,
@@ -148,11 +165,19 @@ def attention(q, q_dtype, num_q_heads, seq_ids, positions, block_tables, num_pag
     n = int(seq_ids.shape[0])
     num_seqs, max_blocks = block_tables.shape
     out = np.zeros((n, num_q_heads, head_dim), dtype=np.float64)
-    st = lib().oracle_attention(n, _ptr(q), q_dtype, num_q_heads, _ptr(seq_ids), _ptr(positions),
-                                _ptr(block_tables), num_seqs, max_blocks, num_pages, page_size,
-                                num_kv_heads, head_dim, kv_dtype, float(k_scale), float(v_scale),
-                                _ptr(np.ascontiguousarray(k_pool)), _ptr(np.ascontiguousarray(v_pool)),
-                                float(softmax_scale), _ptr(out), int(n_threads))
+    if np.ndim(k_scale) or np.ndim(v_scale):  # one scale per kv head
+        ks, vs = _head_scales(k_scale, num_kv_heads), _head_scales(v_scale, num_kv_heads)
+        st = lib().oracle_attention_h(n, _ptr(q), q_dtype, num_q_heads, _ptr(seq_ids), _ptr(positions),
+                                      _ptr(block_tables), num_seqs, max_blocks, num_pages, page_size,
+                                      num_kv_heads, head_dim, kv_dtype, _ptr(ks), _ptr(vs),
+                                      _ptr(np.ascontiguousarray(k_pool)), _ptr(np.ascontiguousarray(v_pool)),
+                                      float(softmax_scale), _ptr(out), int(n_threads))
+    else:
+        st = lib().oracle_attention(n, _ptr(q), q_dtype, num_q_heads, _ptr(seq_ids), _ptr(positions),
+                                    _ptr(block_tables), num_seqs, max_blocks, num_pages, page_size,
+                                    num_kv_heads, head_dim, kv_dtype, float(k_scale), float(v_scale),
+                                    _ptr(np.ascontiguousarray(k_pool)), _ptr(np.ascontiguousarray(v_pool)),
+                                    float(softmax_scale), _ptr(out), int(n_threads))
     if st != 0:
         raise ValueError(f"oracle_attention failed with status {st}")
     return out

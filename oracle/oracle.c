@@ -19,7 +19,9 @@
  *   - "GPU inference engine engineering", section "The same bits in any batch":
  *     BF16 key/value storage with round-to-nearest-even.
  *   - "Engines for the card you have", section "One checkpoint, many engines":
- *     an FP8 key/value cache with calibration (a per-tensor scale here).
+ *     an FP8 key/value cache with calibration.  The pages leave the calibration's
+ *     granularity open; the oracle takes a per-tensor scale, or one scale per
+ *     KV head.
  *
  * Readings where the pages are silent (each listed in the design doc):
  *   - a row at position p attends keys 0..p inclusive (causal, own token included);
@@ -190,11 +192,11 @@ static int store_pool(void *pool, int kv_dtype, int64_t i, const void *src, int 
  * slot p % P, for every kv head and every element, in row order.
  * Returns 0, or -1 if a row's sequence, position or page is out of range (the
  * rows before it are written), or -2 for an unsupported dtype pair.           */
-int oracle_append(int32_t n_rows, const void *k_new, const void *v_new, int32_t in_dtype,
-                  const int32_t *seq_ids, const int32_t *positions, const int32_t *block_tables,
-                  int32_t num_seqs, int32_t max_blocks, int32_t num_pages, int32_t page_size,
-                  int32_t num_kv_heads, int32_t head_dim, int32_t kv_dtype, float k_scale,
-                  float v_scale, void *k_pool, void *v_pool)
+int oracle_append_h(int32_t n_rows, const void *k_new, const void *v_new, int32_t in_dtype,
+                    const int32_t *seq_ids, const int32_t *positions, const int32_t *block_tables,
+                    int32_t num_seqs, int32_t max_blocks, int32_t num_pages, int32_t page_size,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t kv_dtype, const float *k_scales,
+                    const float *v_scales, void *k_pool, void *v_pool)
 {
     const int P = page_size, H = num_kv_heads, D = head_dim;
     for (int32_t r = 0; r < n_rows; ++r) {
@@ -209,12 +211,38 @@ int oracle_append(int32_t n_rows, const void *k_new, const void *v_new, int32_t 
             for (int d = 0; d < D; ++d) {
                 int64_t dst = (((int64_t)page * H + h) * P + slot) * D + d;
                 int64_t src = ((int64_t)r * H + h) * D + d;
-                if (store_pool(k_pool, kv_dtype, dst, k_new, in_dtype, src, k_scale) ||
-                    store_pool(v_pool, kv_dtype, dst, v_new, in_dtype, src, v_scale))
+                if (store_pool(k_pool, kv_dtype, dst, k_new, in_dtype, src, k_scales[h]) ||
+                    store_pool(v_pool, kv_dtype, dst, v_new, in_dtype, src, v_scales[h]))
                     return -2;
             }
     }
     return 0;
+}
+
+/* The same with one scale for every kv head (a per-tensor scale). */
+int oracle_append(int32_t n_rows, const void *k_new, const void *v_new, int32_t in_dtype,
+                  const int32_t *seq_ids, const int32_t *positions, const int32_t *block_tables,
+                  int32_t num_seqs, int32_t max_blocks, int32_t num_pages, int32_t page_size,
+                  int32_t num_kv_heads, int32_t head_dim, int32_t kv_dtype, float k_scale,
+                  float v_scale, void *k_pool, void *v_pool)
+{
+    if (num_kv_heads <= 0)
+        return -2;
+    float *ks = (float *)malloc(sizeof(float) * (size_t)num_kv_heads);
+    float *vs = (float *)malloc(sizeof(float) * (size_t)num_kv_heads);
+    int st = -3;
+    if (ks && vs) {
+        for (int h = 0; h < num_kv_heads; ++h) {
+            ks[h] = k_scale;
+            vs[h] = v_scale;
+        }
+        st = oracle_append_h(n_rows, k_new, v_new, in_dtype, seq_ids, positions, block_tables, num_seqs,
+                             max_blocks, num_pages, page_size, num_kv_heads, head_dim, kv_dtype, ks, vs,
+                             k_pool, v_pool);
+    }
+    free(ks);
+    free(vs);
+    return st;
 }
 
 /* -------------------------------------------------------------- attention -- */
@@ -225,7 +253,7 @@ typedef struct {
     int32_t q_dtype, num_q_heads;
     const int32_t *seq_ids, *positions, *block_tables;
     int32_t num_seqs, max_blocks, num_pages, page_size, num_kv_heads, head_dim, kv_dtype;
-    float k_scale, v_scale;
+    const float *k_scales, *v_scales;  /* per kv head */
     const void *k_pool, *v_pool;
     double softmax_scale;
     double *out;
@@ -276,7 +304,7 @@ static void attention_rows(attn_args *a)
                 double dot = 0.0;
                 for (int d = 0; d < D; ++d)
                     dot += (double)load_as_f32(a->q, a->q_dtype, qoff + d) *
-                           load_pool(a->k_pool, a->kv_dtype, base + d, a->k_scale);
+                           load_pool(a->k_pool, a->kv_dtype, base + d, a->k_scales[h]);
                 score[t] = a->softmax_scale * dot;
                 if (score[t] > m)
                     m = score[t];
@@ -289,7 +317,7 @@ static void attention_rows(attn_args *a)
                 int64_t base = (((int64_t)page_of[t / P] * H + h) * P + t % P) * D;
                 z += w;
                 for (int d = 0; d < D; ++d)
-                    acc[d] += w * load_pool(a->v_pool, a->kv_dtype, base + d, a->v_scale);
+                    acc[d] += w * load_pool(a->v_pool, a->kv_dtype, base + d, a->v_scales[h]);
             }
             for (int d = 0; d < D; ++d)
                 a->out[qoff + d] = acc[d] / z;
@@ -311,12 +339,12 @@ static void *attention_thread(void *p)
  * host memory ran out.  softmax_scale <= 0 means 1/sqrt(head_dim).
  * n_threads > 1 splits the rows into contiguous ranges, one per thread; each
  * row's arithmetic is the same whichever thread runs it.                     */
-int oracle_attention(int32_t n_rows, const void *q, int32_t q_dtype, int32_t num_q_heads,
-                     const int32_t *seq_ids, const int32_t *positions, const int32_t *block_tables,
-                     int32_t num_seqs, int32_t max_blocks, int32_t num_pages, int32_t page_size,
-                     int32_t num_kv_heads, int32_t head_dim, int32_t kv_dtype, float k_scale,
-                     float v_scale, const void *k_pool, const void *v_pool, double softmax_scale,
-                     double *out, int32_t n_threads)
+int oracle_attention_h(int32_t n_rows, const void *q, int32_t q_dtype, int32_t num_q_heads,
+                       const int32_t *seq_ids, const int32_t *positions, const int32_t *block_tables,
+                       int32_t num_seqs, int32_t max_blocks, int32_t num_pages, int32_t page_size,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t kv_dtype, const float *k_scales,
+                       const float *v_scales, const void *k_pool, const void *v_pool, double softmax_scale,
+                       double *out, int32_t n_threads)
 {
     if (n_rows < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || page_size <= 0 ||
         head_dim <= 0 || (q_dtype != OR_F32 && q_dtype != OR_BF16) ||
@@ -351,8 +379,8 @@ int oracle_attention(int32_t n_rows, const void *q, int32_t q_dtype, int32_t num
         a->num_kv_heads = num_kv_heads;
         a->head_dim = head_dim;
         a->kv_dtype = kv_dtype;
-        a->k_scale = k_scale;
-        a->v_scale = v_scale;
+        a->k_scales = k_scales;
+        a->v_scales = v_scales;
         a->k_pool = k_pool;
         a->v_pool = v_pool;
         a->softmax_scale = softmax_scale;
@@ -385,4 +413,31 @@ int oracle_attention(int32_t n_rows, const void *q, int32_t q_dtype, int32_t num
 size_t oracle_elt_size(int32_t dtype)
 {
     return elt_size(dtype);
+}
+
+/* The same with one scale for every kv head (a per-tensor scale). */
+int oracle_attention(int32_t n_rows, const void *q, int32_t q_dtype, int32_t num_q_heads,
+                     const int32_t *seq_ids, const int32_t *positions, const int32_t *block_tables,
+                     int32_t num_seqs, int32_t max_blocks, int32_t num_pages, int32_t page_size,
+                     int32_t num_kv_heads, int32_t head_dim, int32_t kv_dtype, float k_scale,
+                     float v_scale, const void *k_pool, const void *v_pool, double softmax_scale,
+                     double *out, int32_t n_threads)
+{
+    if (num_kv_heads <= 0)
+        return -2;
+    float *ks = (float *)malloc(sizeof(float) * (size_t)num_kv_heads);
+    float *vs = (float *)malloc(sizeof(float) * (size_t)num_kv_heads);
+    int st = -3;
+    if (ks && vs) {
+        for (int h = 0; h < num_kv_heads; ++h) {
+            ks[h] = k_scale;
+            vs[h] = v_scale;
+        }
+        st = oracle_attention_h(n_rows, q, q_dtype, num_q_heads, seq_ids, positions, block_tables, num_seqs,
+                                max_blocks, num_pages, page_size, num_kv_heads, head_dim, kv_dtype, ks, vs,
+                                k_pool, v_pool, softmax_scale, out, n_threads);
+    }
+    free(ks);
+    free(vs);
+    return st;
 }

@@ -454,3 +454,47 @@ def test_page_counts_printed_for_32_token_pages():
     wl = W.mixed_step(n_decode=2, ctx_hi=100)
     cs = wl.num_seqs - 1
     assert int((wl.block_tables[cs] >= 0).sum()) == 84
+
+
+def test_per_head_scales_equal_per_tensor_on_rescaled_inputs():
+    """One fp8 scale per kv head.  With power-of-two scales s_h (keys) and t_h
+    (values), appending K = s_h * y and V = t_h * z with the per-head scales
+    stores the same codes as appending y and z with scale 1; attention then
+    equals scale-1 attention with each query head of group h multiplied by s_h,
+    times t_h.  A head index mixed up anywhere (encode, key decode, value
+    decode) breaks one of the two equalities."""
+    rng = np.random.default_rng(12)
+    Hkv, G, D, P, npg = 3, 2, 16, 8, 12
+    s_h = np.array([2.0 ** -3, 2.0 ** -6, 2.0 ** 1], np.float32)
+    t_h = np.array([2.0 ** 2, 2.0 ** -5, 2.0 ** -1], np.float32)
+    ctx = [5, 17, 30]
+    bt = np.full((3, 4), -1, np.int32)
+    bt[0, :1], bt[1, :3], bt[2, :4] = [7], [0, 3, 9], [1, 2, 4, 11]
+    seq = np.repeat(np.arange(3, dtype=np.int32), ctx)
+    pos = np.concatenate([np.arange(c, dtype=np.int32) for c in ctx])
+    y = W.to_bf16_bits(rng.standard_normal((len(seq), Hkv, D)).astype(np.float32) * 40)
+    z = W.to_bf16_bits(rng.standard_normal((len(seq), Hkv, D)).astype(np.float32) * 40)
+    yf, zf = W.bf16_bits_to_f32(y), W.bf16_bits_to_f32(z)
+    x = W.to_bf16_bits(yf * s_h[None, :, None])  # exact: powers of two
+    u = W.to_bf16_bits(zf * t_h[None, :, None])
+    pools = {}
+    for name, (kin, vin, ks, vs) in {"per_head": (x, u, s_h, t_h), "unit": (y, z, 1.0, 1.0)}.items():
+        kp = np.zeros((npg, Hkv, P, D), np.uint8)
+        vp = np.zeros((npg, Hkv, P, D), np.uint8)
+        assert oracle.append(kin, vin, W.BF16, seq, pos, bt, npg, P, Hkv, D, W.E4M3, ks, vs, kp, vp) == 0
+        pools[name] = (kp, vp)
+    assert pools["per_head"][0].tobytes() == pools["unit"][0].tobytes()
+    assert pools["per_head"][1].tobytes() == pools["unit"][1].tobytes()
+    q = rng.standard_normal((3, Hkv * G, D)).astype(np.float32)
+    qs = (q * np.repeat(s_h, G)[None, :, None]).astype(np.float32)
+    rows = np.arange(3, dtype=np.int32)
+    last = np.array(ctx, np.int32) - 1
+    kp, vp = pools["per_head"]
+    a = oracle.attention(q, W.F32, Hkv * G, rows, last, bt, npg, P, Hkv, D, W.E4M3, s_h, t_h, kp, vp)
+    b = oracle.attention(qs, W.F32, Hkv * G, rows, last, bt, npg, P, Hkv, D, W.E4M3, 1.0, 1.0, kp, vp)
+    np.testing.assert_allclose(a, b * np.repeat(t_h, G)[None, :, None], rtol=1e-13, atol=0)
+    # and the per-head path with equal scales is the per-tensor path, bit for bit
+    c = oracle.attention(q, W.F32, Hkv * G, rows, last, bt, npg, P, Hkv, D, W.E4M3, np.full(Hkv, 0.5, np.float32),
+                         np.full(Hkv, 0.25, np.float32), kp, vp)
+    d = oracle.attention(q, W.F32, Hkv * G, rows, last, bt, npg, P, Hkv, D, W.E4M3, 0.5, 0.25, kp, vp)
+    assert c.tobytes() == d.tobytes()

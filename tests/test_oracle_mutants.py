@@ -36,6 +36,15 @@ MUTANTS = [
      "load_as_f32(src, in_dtype, j) * scale;"),
     ("overflow to NaN instead of saturating", "if (a >= 448.0)\n        return sign | 0x7e;",
      "if (a >= 448.0)\n        return sign | 0x7f;"),
+    ("per-head key scale of the wrong head on append",
+     "store_pool(k_pool, kv_dtype, dst, k_new, in_dtype, src, k_scales[h])",
+     "store_pool(k_pool, kv_dtype, dst, k_new, in_dtype, src, k_scales[(h + 1) % H])"),
+    ("per-head value scale of the wrong head on decode",
+     "load_pool(a->v_pool, a->kv_dtype, base + d, a->v_scales[h]);",
+     "load_pool(a->v_pool, a->kv_dtype, base + d, a->v_scales[0]);"),
+    ("per-head key scale of the wrong head on decode",
+     "load_pool(a->k_pool, a->kv_dtype, base + d, a->k_scales[h]);",
+     "load_pool(a->k_pool, a->kv_dtype, base + d, a->k_scales[H - 1 - h]);"),
 ]
 
 PINS = [
@@ -51,6 +60,7 @@ PINS = [
     lambda: T.test_e4m3_encode_decode_identity_and_saturation(),
     lambda: T.test_e4m3_encoder_matches_torch_in_non_saturating_range(),
     lambda: T.test_fp8_append_divides_by_scale_in_binary32(),
+    lambda: T.test_per_head_scales_equal_per_tensor_on_rescaled_inputs(),
 ]
 
 
