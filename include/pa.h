@@ -62,7 +62,7 @@ typedef enum {
 
 typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
 
-/* Pool geometry.  page_size in {16, 32, 64}; head_dim in {64, 128};
+/* Pool geometry.  page_size in {16, 32, 64, 128, 256}; head_dim in {64, 128};
  * kv_dtype PA_F32, PA_BF16 or PA_FP8_E4M3.  k_scale / v_scale are the fp8
  * per-tensor scales ("Engines for the card you have", section "One checkpoint,
  * many engines": an FP8 key/value cache, calibrated): a stored code c means
@@ -103,6 +103,17 @@ pa_status pa_pool_create(const pa_pool_desc *desc, void *k_pool, void *v_pool, p
 
 /* Free the host object (not the device buffers).  NULL is allowed. */
 void pa_pool_destroy(pa_pool *pool);
+
+/* One fp8 scale per kv head instead of the descriptor's per-tensor scales
+ * ("Engines for the card you have", section "One checkpoint, many engines":
+ * a calibrated FP8 key/value cache; the calibration's granularity is the
+ * caller's).  k_scales, v_scales: HOST arrays of num_kv_heads floats, copied;
+ * kv head h stores e4m3_satfinite_rne(x / k_scales[h]) and decodes
+ * value(c) * k_scales[h] (likewise V).  Both NULL: back to the per-tensor
+ * scales.  Errors: PA_ERR_INVALID_ARG (one array NULL, a pool that is not
+ * fp8, a scale not finite and positive), PA_ERR_UNSUPPORTED (more than 64 kv
+ * heads).  Takes effect for calls made after it. */
+pa_status pa_pool_set_head_scales(pa_pool *pool, const float *k_scales, const float *v_scales);
 
 /* K/V append ("GPU inference engine engineering", "Batching without running
  * out of cache"): for each row r, kv head h and element d,

@@ -70,6 +70,8 @@ def load(path: str = LIB_PATH):
         L.pa_pool_create.restype = st
         L.pa_pool_destroy.argtypes = [vp]
         L.pa_pool_destroy.restype = None
+        L.pa_pool_set_head_scales.argtypes = [vp, vp, vp]
+        L.pa_pool_set_head_scales.restype = st
         L.pa_append_kv.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, i32, i32, vp, vp]
         L.pa_append_kv.restype = st
         L.pa_attention_workspace_bytes.argtypes = [vp, i32, i32, i32, ctypes.POINTER(Chunk), i32]
@@ -167,19 +169,28 @@ def pool_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int,
 class Pool:
     """A paged K/V pool over two caller-owned device tensors [num_pages, Hkv, P, D]."""
 
-    def __init__(self, k_pool, v_pool, k_scale: float = 1.0, v_scale: float = 1.0):
+    def __init__(self, k_pool, v_pool, k_scale=1.0, v_scale=1.0):
+        """k_scale / v_scale: fp8 scales, one float (per tensor) or one per kv head."""
+        import numpy as np
         if k_pool.shape != v_pool.shape or k_pool.dim() != 4 or k_pool.dtype != v_pool.dtype:
             raise ValueError("k_pool and v_pool must be matching [num_pages, Hkv, P, D] tensors")
         self.k_pool, self.v_pool = k_pool, v_pool
         n, h, p, d = k_pool.shape
         self.num_pages, self.num_kv_heads, self.page_size, self.head_dim = int(n), int(h), int(p), int(d)
         self.kv_dtype = _dtype_code(k_pool)
-        self.k_scale, self.v_scale = float(k_scale), float(v_scale)
+        per_head = np.ndim(k_scale) > 0 or np.ndim(v_scale) > 0
+        self.k_scale = np.asarray(k_scale, np.float32) if per_head else float(k_scale)
+        self.v_scale = np.asarray(v_scale, np.float32) if per_head else float(v_scale)
         self.desc = PoolDesc(self.num_pages, self.page_size, self.num_kv_heads, self.head_dim, self.kv_dtype,
-                             self.k_scale, self.v_scale)
+                             1.0 if per_head else self.k_scale, 1.0 if per_head else self.v_scale)
         handle = ctypes.c_void_p()
         _check(load().pa_pool_create(ctypes.byref(self.desc), _ptr(k_pool), _ptr(v_pool), ctypes.byref(handle)))
         self._h = handle
+        if per_head:
+            ks = np.ascontiguousarray(np.broadcast_to(self.k_scale, (self.num_kv_heads,)), np.float32)
+            vs = np.ascontiguousarray(np.broadcast_to(self.v_scale, (self.num_kv_heads,)), np.float32)
+            _check(load().pa_pool_set_head_scales(self._h, ks.ctypes.data_as(ctypes.c_void_p),
+                                                  vs.ctypes.data_as(ctypes.c_void_p)))
 
     @property
     def handle(self):

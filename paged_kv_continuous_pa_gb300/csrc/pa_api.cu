@@ -16,6 +16,8 @@
 
 struct pa_pool {
   pa_pool_desc desc;
+  bool head_scales;  // fp8 scales per kv head (pa_pool_set_head_scales)
+  float k_scale_h[pa::kMaxHeadScales], v_scale_h[pa::kMaxHeadScales];
   void* k;
   void* v;
   bool maps_ready;   // kmap / vmap encoded (on first use by a tensor-map path)
@@ -139,9 +141,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // The pool as a 2-D tensor [num_pages * Hkv * P rows][D] with 128-byte
 // swizzle, the layout the tensor-core paths read.  bf16 pools (the prefill
-// tile path): boxes of 64 elements x P rows, one page of one kv head, half or
-// all of the head dim.  e4m3 pools with D = 128 (the tensor-core decode
-// units): the rows as 128 bytes, boxes of 128 bytes x min(P, 32) rows.
+// tile path): boxes of 64 elements x min(P, 64) rows of one page of one kv
+// head, half or all of the head dim.  e4m3 pools with D = 128 (the
+// tensor-core decode units): the rows as 128 bytes, boxes of 128 bytes x
+// min(P, 32) rows.
 pa_status encode_pool_maps(pa_pool* pool) {
   if (pool->maps_ready) return PA_OK;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -153,8 +156,8 @@ pa_status encode_pool_maps(pa_pool* pool) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim),
                         static_cast<cuuint64_t>(d.num_pages) * d.num_kv_heads * d.page_size};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * elt_bytes(d.kv_dtype)};
-  cuuint32_t box[2] = {fp8 ? 128u : 64u,
-                       static_cast<cuuint32_t>(fp8 && d.page_size > 32 ? 32 : d.page_size)};
+  const int box_rows = fp8 ? (d.page_size > 32 ? 32 : d.page_size) : (d.page_size > 64 ? 64 : d.page_size);
+  cuuint32_t box[2] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   for (int i = 0; i < 2; ++i) {
@@ -174,8 +177,8 @@ pa_status check_desc(const pa_pool_desc* d) {
                 d->num_pages, d->num_kv_heads, d->page_size, d->head_dim);
   if (d->kv_dtype != PA_F32 && d->kv_dtype != PA_BF16 && d->kv_dtype != PA_FP8_E4M3)
     return fail(PA_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(d->kv_dtype));
-  if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
-    return fail(PA_ERR_UNSUPPORTED, "page_size %d not in {16, 32, 64}", d->page_size);
+  if (d->page_size < 16 || d->page_size > 256 || (d->page_size & (d->page_size - 1)) != 0)
+    return fail(PA_ERR_UNSUPPORTED, "page_size %d not in {16, 32, 64, 128, 256}", d->page_size);
   if (d->head_dim != 64 && d->head_dim != 128)
     return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}", d->head_dim);
   if (d->kv_dtype == PA_FP8_E4M3 &&
@@ -229,8 +232,11 @@ pa_status build_append(const pa_pool* pool, int32_t n_rows, const void* k_new, c
   p.D = pool->desc.head_dim;
   p.in_dtype = in_dtype == PA_F32 ? pa::KV_F32 : pa::KV_BF16;
   p.kv_dtype = static_cast<int32_t>(pool->desc.kv_dtype);
-  p.k_scale = pool->desc.k_scale;
-  p.v_scale = pool->desc.v_scale;
+  p.head_scales = pool->head_scales ? 1 : 0;
+  for (int h = 0; h < (pool->head_scales ? pool->desc.num_kv_heads : 1); ++h) {
+    p.k_scale_h[h] = pool->head_scales ? pool->k_scale_h[h] : pool->desc.k_scale;
+    p.v_scale_h[h] = pool->head_scales ? pool->v_scale_h[h] : pool->desc.v_scale;
+  }
   p.status = status_dev;
   *out = p;
   return PA_OK;
@@ -287,7 +293,6 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
     if (!aligned(workspace, 256)) return fail(PA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   }
   const double sm = softmax_scale > 0.f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt(static_cast<double>(d.head_dim));
-  const double k_scale = d.kv_dtype == PA_FP8_E4M3 ? static_cast<double>(d.k_scale) : 1.0;
 
   pa::AttnParams p{};
   p.k_pool = pool->k;
@@ -308,8 +313,14 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
   p.q_is_bf16 = q_dtype == PA_BF16;
   p.split_tokens = g_split_tokens;
   p.max_splits = pl.max_splits;
-  p.qk_scale_log2 = static_cast<float>(sm * k_scale * 1.4426950408889634073599246810018921);  // log2(e)
-  p.v_scale = d.kv_dtype == PA_FP8_E4M3 ? d.v_scale : 1.0f;
+  // per kv head (or entry 0 for all): softmax scale * k scale * log2(e), and the v scale
+  p.head_scales = pool->head_scales ? 1 : 0;
+  for (int h = 0; h < (pool->head_scales ? d.num_kv_heads : 1); ++h) {
+    const bool fp8 = d.kv_dtype == PA_FP8_E4M3;
+    const double ks = fp8 ? static_cast<double>(pool->head_scales ? pool->k_scale_h[h] : d.k_scale) : 1.0;
+    p.qk_scale_log2_h[h] = static_cast<float>(sm * ks * 1.4426950408889634073599246810018921);  // log2(e)
+    p.v_scale_h[h] = fp8 ? (pool->head_scales ? pool->v_scale_h[h] : d.v_scale) : 1.0f;
+  }
   if (pl.total > 0) {
     unsigned char* base = static_cast<unsigned char*>(workspace);
     if (pl.max_splits > 1) {
@@ -409,6 +420,7 @@ pa_status pa_pool_create(const pa_pool_desc* desc, void* k_pool, void* v_pool, p
   if (p == nullptr) return fail(PA_ERR_INVALID_ARG, "out of host memory");
   p->desc = *desc;
   if (p->desc.kv_dtype != PA_FP8_E4M3) p->desc.k_scale = p->desc.v_scale = 1.0f;
+  p->head_scales = false;
   p->k = k_pool;
   p->v = v_pool;
   p->maps_ready = false;
@@ -417,6 +429,30 @@ pa_status pa_pool_create(const pa_pool_desc* desc, void* k_pool, void* v_pool, p
 }
 
 void pa_pool_destroy(pa_pool* pool) { delete pool; }
+
+pa_status pa_pool_set_head_scales(pa_pool* pool, const float* k_scales, const float* v_scales) {
+  if (pool == nullptr) return fail(PA_ERR_INVALID_ARG, "pool is NULL");
+  if (k_scales == nullptr && v_scales == nullptr) {
+    pool->head_scales = false;  // back to the per-tensor scales of the pool descriptor
+    return PA_OK;
+  }
+  if (k_scales == nullptr || v_scales == nullptr)
+    return fail(PA_ERR_INVALID_ARG, "give both scale arrays (or neither)");
+  if (pool->desc.kv_dtype != PA_FP8_E4M3) return fail(PA_ERR_INVALID_ARG, "per-head scales apply to fp8 pools only");
+  const int H = pool->desc.num_kv_heads;
+  if (H > pa::kMaxHeadScales)
+    return fail(PA_ERR_UNSUPPORTED, "per-head scales for %d kv heads (at most %d)", H, pa::kMaxHeadScales);
+  for (int h = 0; h < H; ++h)
+    if (!(std::isfinite(k_scales[h]) && k_scales[h] > 0.f && std::isfinite(v_scales[h]) && v_scales[h] > 0.f))
+      return fail(PA_ERR_INVALID_ARG, "scales of kv head %d must be finite and positive (k %g, v %g)", h, k_scales[h],
+                  v_scales[h]);
+  for (int h = 0; h < H; ++h) {
+    pool->k_scale_h[h] = k_scales[h];
+    pool->v_scale_h[h] = v_scales[h];
+  }
+  pool->head_scales = true;
+  return PA_OK;
+}
 
 pa_status pa_append_kv(const pa_pool* pool, int32_t n_rows, const void* k_new, const void* v_new, pa_dtype in_dtype,
                        const int32_t* seq_ids, const int32_t* positions, const int32_t* block_tables,

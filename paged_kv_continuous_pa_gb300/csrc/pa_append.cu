@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
     }
     *reinterpret_cast<uint4*>(static_cast<uint16_t*>(pool) + dst) = make_uint4(o[0], o[1], o[2], o[3]);
   } else {
-    const float scale = is_v ? p.v_scale : p.k_scale;
+    const float scale = is_v ? p.v_scale_h[PA_HEAD(p, h)] : p.k_scale_h[PA_HEAD(p, h)];
     uint32_t o[2] = {0u, 0u};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {

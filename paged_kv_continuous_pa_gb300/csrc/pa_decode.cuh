@@ -416,7 +416,7 @@ __device__ __forceinline__ void decode_finish(const AttnParams& p, bool bad, int
         osum = fmaf(f, red_acc[(w * G + g) * D + d], osum);
       }
       float o = __fdiv_rn(osum, lsum);
-      if (KVT == KV_E4M3) o = __fmul_rn(o, p.v_scale);
+      if (KVT == KV_E4M3) o = __fmul_rn(o, p.v_scale_h[PA_HEAD(p, h)]);
       store_out(p.out, q_bf16, out_row * D + i, bad ? 0.0f : o);
     }
     return;
@@ -485,7 +485,7 @@ __device__ __forceinline__ void decode_finish(const AttnParams& p, bool bad, int
 #pragma unroll 4
       for (int sp = 0; sp < nsplit; ++sp) osum = fmaf(fbuf[g * nsplit + sp], __ldcg(o + static_cast<size_t>(sp) * D), osum);
       float out = __fdiv_rn(osum, fbuf[G * nsplit + g]);
-      if (KVT == KV_E4M3) out = __fmul_rn(out, p.v_scale);
+      if (KVT == KV_E4M3) out = __fmul_rn(out, p.v_scale_h[PA_HEAD(p, h)]);
       store_out(p.out, q_bf16, out_row * D + i, out);
     }
   } else {
@@ -501,7 +501,7 @@ __device__ __forceinline__ void decode_finish(const AttnParams& p, bool bad, int
         osum = fmaf(f, __ldcg(p.ws_o + (slot0 + sp) * D + d), osum);
       }
       float out = __fdiv_rn(osum, lsum);
-      if (KVT == KV_E4M3) out = __fmul_rn(out, p.v_scale);
+      if (KVT == KV_E4M3) out = __fmul_rn(out, p.v_scale_h[PA_HEAD(p, h)]);
       store_out(p.out, q_bf16, out_row * D + i, out);
     }
   }
@@ -612,7 +612,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
         const int vidx = part + LPT * ((i + tok) % NV);
         load_q_vec<EPV>(p.q, q_bf16, qrow + static_cast<size_t>(g) * D + vidx * EPV, st.qr[g][i]);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) st.qr[g][i][e] = __fmul_rn(st.qr[g][i][e], p.qk_scale_log2);
+        for (int e = 0; e < EPV; ++e) st.qr[g][i][e] = __fmul_rn(st.qr[g][i][e], p.qk_scale_log2_h[PA_HEAD(p, h)]);
       }
   }
   float* pbuf = &hdr->p[warp][0][0];

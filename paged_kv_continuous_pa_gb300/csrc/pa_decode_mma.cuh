@@ -248,7 +248,7 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
     const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 126;
     const int shift = min(100, max(-100, e - 15));
     const float down = __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
-    score_scale = __fmul_rn(p.qk_scale_log2, __uint_as_float(static_cast<uint32_t>(127 + shift) << 23));
+    score_scale = __fmul_rn(p.qk_scale_log2_h[PA_HEAD(p, h)], __uint_as_float(static_cast<uint32_t>(127 + shift) << 23));
 #pragma unroll
     for (int kb = 0; kb < 4; ++kb) {
       qf[kb][0] = pack_f16x2(qv[kb][0] * down, qv[kb][1] * down);  // mma0: elements 4t4 + {0,1}
@@ -423,7 +423,7 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
     for (int hh = 0; hh < 2; ++hh) {
       const int head = 2 * t4 + hh;
       if (head < G) {
-        const float r = __fdiv_rn(p.v_scale, lsum[hh]);
+        const float r = __fdiv_rn(p.v_scale_h[PA_HEAD(p, h)], lsum[hh]);
         uint32_t w0[4], w1[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {  // a unit that hit an error writes zeros

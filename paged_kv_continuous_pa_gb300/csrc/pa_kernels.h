@@ -41,6 +41,11 @@ enum KvType { KV_F32 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
 // Device status codes (same values as pa_status in include/pa.h).
 enum { ST_OK = 0, ST_OUT_OF_RANGE = 3, ST_TIMEOUT = 4 };
 
+constexpr int kMaxHeadScales = 64;  // kv heads a pool with per-head fp8 scales may have
+
+// The scale entry of kv head h: per head, or the per-tensor entry 0.
+#define PA_HEAD(p, h) ((p).head_scales ? (h) : 0)
+
 struct AppendParams {
   void* k_pool;
   void* v_pool;
@@ -53,7 +58,8 @@ struct AppendParams {
   int32_t P, Hkv, D;
   int32_t in_dtype;  // KV_F32 or KV_BF16
   int32_t kv_dtype;  // KvType
-  float k_scale, v_scale;
+  int32_t head_scales;  // 1: k_scale_h / v_scale_h hold one scale per kv head; 0: entry 0 holds the per-tensor scale
+  float k_scale_h[kMaxHeadScales], v_scale_h[kMaxHeadScales];
   int32_t* status;
 };
 
@@ -70,8 +76,9 @@ struct AttnParams {
   int32_t q_is_bf16;
   int32_t split_tokens;  // split-KV chunk length (multiple of P)
   int32_t max_splits;    // ceil(max_blocks * P / split_tokens)
-  float qk_scale_log2;   // softmax scale * log2(e) * k_scale (scores live in the log2 domain)
-  float v_scale;         // fp8 value scale, 1 otherwise
+  int32_t head_scales;   // 1: the two arrays below hold one entry per kv head; 0: entry 0 for every head
+  float qk_scale_log2_h[kMaxHeadScales];  // softmax scale * log2(e) * k scale (scores live in the log2 domain)
+  float v_scale_h[kMaxHeadScales];        // fp8 value scale, 1 otherwise
   float* ws_o;           // [n_rows][Hq][max_splits][D] partial accumulators (split rows only)
   float* ws_ml;          // [n_rows][Hq][max_splits][2] partial (max, sum)
   int32_t* ws_count;     // [n_rows][Hkv] finished-split counters, zero between calls

@@ -75,15 +75,17 @@ __device__ __forceinline__ void prefill_load_kv(const AttnParams& p, const CUten
                                                 uint64_t* bar, const int32_t* bt, int j, int h, int fallback_pid) {
   constexpr int NH = D / 64;
   const int P = p.P;
+  const int BR = P < kTileN ? P : kTileN;  // rows of one box: a page, or a 64-key part of a larger page
   mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kTileN * D * 2));
-  for (int k = 0; k < kTileN / P; ++k) {
-    const int jp = (j * kTileN) / P + k;  // logical page
+  for (int k = 0; k < kTileN / BR; ++k) {
+    const int t = j * kTileN + k * BR;  // first key of the box
+    const int jp = t / P;               // logical page
     int pid = jp < p.max_blocks ? __ldg(bt + jp) : -1;
     if (pid < 0 || pid >= p.num_pages) pid = fallback_pid;  // keys past the sequence: masked / zeroed later
-    const int y = (pid * p.Hkv + h) * P;
+    const int y = (pid * p.Hkv + h) * P + t % P;
 #pragma unroll
     for (int half = 0; half < NH; ++half)
-      tc::tma_load_2d(dst + half * PrefillSmem<D>::KH + k * P * 128, map, half * 64, y, bar);
+      tc::tma_load_2d(dst + half * PrefillSmem<D>::KH + k * BR * 128, map, half * 64, y, bar);
   }
 }
 

@@ -54,6 +54,12 @@ def test_pool_create_validation(lib):
     lib.pa_pool_destroy(h)
     assert _create(lib, _desc(head_dim=96))[0] == pa.PA_ERR_UNSUPPORTED
     assert _create(lib, _desc(page_size=8))[0] == pa.PA_ERR_UNSUPPORTED
+    assert _create(lib, _desc(page_size=48))[0] == pa.PA_ERR_UNSUPPORTED  # not a power of two
+    assert _create(lib, _desc(page_size=512))[0] == pa.PA_ERR_UNSUPPORTED
+    for ps in (16, 32, 64, 128, 256):
+        st, h = _create(lib, _desc(page_size=ps))
+        assert st == pa.PA_OK
+        lib.pa_pool_destroy(h)
     assert _create(lib, _desc(num_pages=0))[0] == pa.PA_ERR_INVALID_ARG
     assert _create(lib, _desc(kv_dtype=7))[0] == pa.PA_ERR_INVALID_ARG
     assert _create(lib, _desc(kv_dtype=pa.PA_FP8_E4M3, k_scale=0.0))[0] == pa.PA_ERR_INVALID_ARG
@@ -123,6 +129,27 @@ def test_split_tokens_setting(lib):
         assert lib.pa_set_split_tokens(512) == pa.PA_OK and lib.pa_get_split_tokens() == 512
     finally:
         lib.pa_set_split_tokens(old)
+
+
+def test_head_scales_validation(lib):
+    arr = lambda *v: (ctypes.c_float * len(v))(*v)
+    st, h = _create(lib, _desc(kv_dtype=pa.PA_FP8_E4M3, k_scale=0.5, v_scale=0.5))
+    assert st == pa.PA_OK
+    try:
+        assert lib.pa_pool_set_head_scales(h, arr(0.1, 0.2), arr(0.3, 0.4)) == pa.PA_OK
+        assert lib.pa_pool_set_head_scales(h, None, None) == pa.PA_OK  # back to per tensor
+        assert lib.pa_pool_set_head_scales(h, arr(0.1, 0.2), None) == pa.PA_ERR_INVALID_ARG
+        assert lib.pa_pool_set_head_scales(h, arr(0.1, 0.0), arr(0.3, 0.4)) == pa.PA_ERR_INVALID_ARG
+        assert lib.pa_pool_set_head_scales(h, arr(0.1, 0.2), arr(float("nan"), 0.4)) == pa.PA_ERR_INVALID_ARG
+    finally:
+        lib.pa_pool_destroy(h)
+    st, h = _create(lib, _desc())  # bf16
+    assert lib.pa_pool_set_head_scales(h, arr(0.1, 0.2), arr(0.3, 0.4)) == pa.PA_ERR_INVALID_ARG
+    lib.pa_pool_destroy(h)
+    st, h = _create(lib, _desc(kv_dtype=pa.PA_FP8_E4M3, num_kv_heads=65))
+    many = (ctypes.c_float * 65)(*([0.5] * 65))
+    assert lib.pa_pool_set_head_scales(h, many, many) == pa.PA_ERR_UNSUPPORTED
+    lib.pa_pool_destroy(h)
 
 
 def test_status_strings(lib):

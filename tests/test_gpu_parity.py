@@ -68,7 +68,7 @@ def test_split_sizes_match_oracle(split):
         pa.set_split_tokens(old)
 
 
-@pytest.mark.parametrize("P", [16, 32, 64])
+@pytest.mark.parametrize("P", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("kv_dtype", [W.F32, W.BF16, W.E4M3])
 def test_page_sizes_and_dtypes(P, kv_dtype):
     q_dtype = W.F32 if kv_dtype == W.F32 else W.BF16

@@ -36,7 +36,7 @@ def test_group_sizes(G):
     run_and_check(W.chunked_step(20 + G, [(50, 140, 200)], decode_ctx=[70, 500], Hq=2 * G, Hkv=2), f"G{G}")
 
 
-@pytest.mark.parametrize("D,P", [(64, 16), (64, 64), (128, 16), (128, 64)])
+@pytest.mark.parametrize("D,P", [(64, 16), (64, 64), (128, 16), (128, 64), (128, 128), (64, 256)])
 def test_head_dims_and_pages(D, P):
     run_and_check(W.chunked_step(30 + D + P, [(33, 97, 180)], decode_ctx=[5, 300], Hq=8, Hkv=2, D=D, P=P),
                   f"D{D} P{P}")
