@@ -41,6 +41,7 @@ L2_BYTES = 129 * 1000 * 1000  # GB300 L2
 W_CONFIG_NAMES = ("batched_decode", "mixed_step", "shared_prefix", "long_context", "tiny_decode",
                   "batched_decode_fp8", "long_context_fp8")
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0  # burst
 
 
 def kernel_source_hash() -> str:
@@ -58,6 +59,51 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_tflops():
+    """Dense bf16 peak for a kernel timed alone (burst), measured; else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def prefill_tiles_alone(pa, torch, st, wl, steps: int, stream):
+    """The chunk rows of the step attended alone (one launch of prefill tiles
+    only, after the step's append): tensor-pipe fraction of the tiles.
+    Algorithmic FLOPs: 4 * D per (chunk row, visible key, query head) --
+    Q.K and P.V, one multiply-add each."""
+    import numpy as np
+    rows = np.concatenate([np.arange(b, b + n) for b, n in wl.chunks])
+    flops = 4.0 * wl.D * wl.Hq * float(np.sum(wl.positions[rows].astype(np.int64) + 1))
+    idx = torch.as_tensor(rows, dtype=torch.long, device=st.q.device)
+    q = st.q[idx].contiguous()
+    out = torch.empty_like(q)
+    seq, pos = st.seq_ids[idx].contiguous(), st.positions[idx].contiguous()
+    starts, b = [], 0
+    for _, n in wl.chunks:
+        starts.append((b, n))
+        b += n
+    wsb = pa.workspace_bytes(st.pool, len(rows), wl.Hq, wl.max_blocks, starts)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=q.device) if wsb else None
+    call = lambda: pa.attention(st.pool, q, seq, pos, st.block_tables, out, chunks=starts,
+                                softmax_scale=wl.softmax_scale, workspace=ws, status=st.status, stream=stream)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, e in ev:
+        a.record(stream)
+        call()
+        e.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(e) for a, e in ev)
+    peak, kind = measured_bf16_tflops()
+    tflops = flops / (ms / 1e3) / 1e12
+    return {"gflop": flops / 1e9, "ms": ms, "tflops": tflops, "peak_tflops": peak, "frac": tflops / peak,
+            "peak_source": f"{kind} (MEASURED_PEAKS.json bf16_tflops, burst)", "kernel": "mixed_kernel tiles only"}
 
 
 def profiled_traffic(workload: str, src_hash: str):
@@ -368,6 +414,9 @@ def run_ours(args):
     src_hash = kernel_source_hash()
     traffic = profiled_traffic(args.workload, src_hash)
     kv_gbs = kv_unique / (att_avg_ms / 1e3) / 1e9
+    tiles = None
+    if attention_kernel_name(wl) == "mixed_kernel":
+        tiles = prefill_tiles_alone(pa, torch, st, wl, max(10, min(args.steps, 50)), stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -397,6 +446,7 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
             "gpu_launches": launches,
+            **({"prefill_tiles": tiles} if tiles else {}),
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
         }
