@@ -273,9 +273,13 @@ def attention_kernel_name(wl) -> str:
     """The kernel pa_attention launches for this workload's decode rows."""
     import workloads as W
     G = wl.Hq // wl.Hkv
+    if wl.chunks and wl.kv_dtype == W.BF16 and wl.q_dtype == W.BF16:
+        return "mixed_kernel"
     if wl.kv_dtype == W.E4M3 and wl.D == 128 and 1 <= G <= 8 and wl.q_dtype == W.BF16:
         return "decode_mma_kernel"
-    return "mixed_kernel" if wl.chunks and wl.kv_dtype == W.BF16 and wl.q_dtype == W.BF16 else "decode_kernel"
+    if wl.kv_dtype == W.BF16 and wl.D == 128 and 3 <= G <= 8 and wl.q_dtype == W.BF16:
+        return "decode_mma_bf16_kernel"
+    return "decode_kernel"
 
 
 def run_ours(args):

@@ -20,9 +20,12 @@ struct pa_pool {
   float k_scale_h[pa::kMaxHeadScales], v_scale_h[pa::kMaxHeadScales];
   void* k;
   void* v;
-  bool maps_ready;   // kmap / vmap encoded (on first use by a tensor-map path)
-  CUtensorMap kmap;  // 2-D views of the pools for tensor-map copies
+  bool tile_maps_ready;  // kmap / vmap encoded (on first use by the prefill tile path)
+  bool dec_maps_ready;   // kmap_dec / vmap_dec encoded (on first use by tensor-core decode units)
+  CUtensorMap kmap;      // 2-D views of the pools for tensor-map copies
   CUtensorMap vmap;
+  CUtensorMap kmap_dec;
+  CUtensorMap vmap_dec;
 };
 
 namespace {
@@ -140,34 +143,50 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // The pool as a 2-D tensor [num_pages * Hkv * P rows][D] with 128-byte
-// swizzle, the layout the tensor-core paths read.  bf16 pools (the prefill
-// tile path): boxes of 64 elements x min(P, 64) rows of one page of one kv
-// head, half or all of the head dim.  e4m3 pools with D = 128 (the
-// tensor-core decode units): the rows as 128 bytes, boxes of 128 bytes x
-// min(P, 32) rows.
-pa_status encode_pool_maps(pa_pool* pool) {
-  if (pool->maps_ready) return PA_OK;
+// swizzle, the layout the tensor-core paths read, boxes of `cols` elements x
+// `rows` rows (one page of one kv head, or a part of it).
+pa_status encode_map_pair(pa_pool* pool, CUtensorMap* km, CUtensorMap* vm, uint32_t cols, uint32_t rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const pa_pool_desc& d = pool->desc;
   const bool fp8 = d.kv_dtype == PA_FP8_E4M3;
-  if (!(d.kv_dtype == PA_BF16 || (fp8 && d.head_dim == 128)))
-    return fail(PA_ERR_UNSUPPORTED, "no tensor-map view for this pool's dtype / head_dim");
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim),
                         static_cast<cuuint64_t>(d.num_pages) * d.num_kv_heads * d.page_size};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * elt_bytes(d.kv_dtype)};
-  const int box_rows = fp8 ? (d.page_size > 32 ? 32 : d.page_size) : (d.page_size > 64 ? 64 : d.page_size);
-  cuuint32_t box[2] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {cols, rows};
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   for (int i = 0; i < 2; ++i) {
-    CUresult r = enc(i == 0 ? &pool->kmap : &pool->vmap, ty, 2, i == 0 ? pool->k : pool->v,
-                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(i == 0 ? km : vm, ty, 2, i == 0 ? pool->k : pool->v, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
   }
-  pool->maps_ready = true;
   return PA_OK;
+}
+
+// bf16 pools, prefill tiles: 64 elements x min(P, 64) rows (half or all of the head dim).
+pa_status encode_tile_maps(pa_pool* pool) {
+  if (pool->tile_maps_ready) return PA_OK;
+  if (pool->desc.kv_dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "the tile path reads bf16 pools");
+  const int P = pool->desc.page_size;
+  const pa_status st = encode_map_pair(pool, &pool->kmap, &pool->vmap, 64u, static_cast<uint32_t>(P > 64 ? 64 : P));
+  if (st == PA_OK) pool->tile_maps_ready = true;
+  return st;
+}
+
+// D = 128 pools, tensor-core decode units: bf16 boxes of 64 elements x min(P, 32)
+// rows (one head-dim half), e4m3 boxes of 128 bytes x min(P, 32) rows.
+pa_status encode_decode_maps(pa_pool* pool) {
+  if (pool->dec_maps_ready) return PA_OK;
+  const pa_pool_desc& d = pool->desc;
+  if (d.head_dim != 128 || (d.kv_dtype != PA_BF16 && d.kv_dtype != PA_FP8_E4M3))
+    return fail(PA_ERR_UNSUPPORTED, "no tensor-core decode view for this pool's dtype / head_dim");
+  const int P = d.page_size;
+  const pa_status st = encode_map_pair(pool, &pool->kmap_dec, &pool->vmap_dec, d.kv_dtype == PA_BF16 ? 64u : 128u,
+                                       static_cast<uint32_t>(P > 32 ? 32 : P));
+  if (st == PA_OK) pool->dec_maps_ready = true;
+  return st;
 }
 
 pa_status check_desc(const pa_pool_desc* d) {
@@ -344,7 +363,7 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
   // Chunks long enough for the tensor-core tile path (bf16 q and K/V): their
   // rows run there; rows of other chunks run as decode rows.
   if (pl.n_tile > 0) {
-    pa_status st = encode_pool_maps(const_cast<pa_pool*>(pool));
+    pa_status st = encode_tile_maps(const_cast<pa_pool*>(pool));
     if (st != PA_OK) return st;
     p.kmap = pool->kmap;
     p.vmap = pool->vmap;
@@ -362,15 +381,18 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
     p.n_prefill_ctas = pl.cta_begin[pl.n_tile];
   }
 
-  // e4m3 pools whose query-head group makes Q.K and P.V small contractions:
-  // tensor-core decode units, reading stages through the pool's tensor maps.
-  const bool mma_decode = d.kv_dtype == PA_FP8_E4M3 && p.n_prefill_ctas == 0 &&
-                          pa::decode_e4m3_mma_eligible(d.head_dim, G, q_dtype == PA_BF16);
-  if (mma_decode) {
-    pa_status st = encode_pool_maps(const_cast<pa_pool*>(pool));
+  // Tensor-core decode units (chosen by pool dtype, head_dim, G and the query
+  // dtype alone, so a row's bits never depend on the rest of the batch): e4m3
+  // pools with D = 128, bf16 pools with D = 128 and G >= 3 (also inside the
+  // mixed launch).  They read stages through the pool's decode tensor maps.
+  const bool q16 = q_dtype == PA_BF16;
+  const bool mma_e4m3 = d.kv_dtype == PA_FP8_E4M3 && pa::decode_e4m3_mma_eligible(d.head_dim, G, q16);
+  const bool mma_bf16 = d.kv_dtype == PA_BF16 && pa::decode_bf16_mma_eligible(d.head_dim, G, q16);
+  if (mma_e4m3 || mma_bf16) {
+    pa_status st = encode_decode_maps(const_cast<pa_pool*>(pool));
     if (st != PA_OK) return st;
-    p.kmap = pool->kmap;
-    p.vmap = pool->vmap;
+    p.kmap_dec = pool->kmap_dec;
+    p.vmap_dec = pool->vmap_dec;
   }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -382,16 +404,15 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
   cudaError_t e = cudaErrorNotSupported;
   if (p.n_prefill_ctas > 0) {
     e = pa::launch_mixed_bf16(p, s);
+  } else if (mma_e4m3) {
+    e = pa::launch_decode_e4m3_mma(p, s);
+  } else if (mma_bf16) {
+    e = pa::launch_decode_bf16_mma(p, s);
   } else {
-    // the tensor-core units decline a grid beyond their limits (more than
-    // 65535 splits a row): the SIMT units take it
-    if (mma_decode) e = pa::launch_decode_e4m3_mma(p, s);
-    if (e == cudaErrorNotSupported) {
-      switch (d.kv_dtype) {
-        case PA_F32: e = pa::launch_decode_f32(p, s); break;
-        case PA_BF16: e = pa::launch_decode_bf16(p, s); break;
-        default: e = pa::launch_decode_e4m3(p, s); break;
-      }
+    switch (d.kv_dtype) {
+      case PA_F32: e = pa::launch_decode_f32(p, s); break;
+      case PA_BF16: e = pa::launch_decode_bf16(p, s); break;
+      default: e = pa::launch_decode_e4m3(p, s); break;
     }
   }
   if (e == cudaErrorNotSupported) return fail(PA_ERR_UNSUPPORTED, "no decode kernel for head_dim %d, group %d", d.head_dim, G);
@@ -423,7 +444,8 @@ pa_status pa_pool_create(const pa_pool_desc* desc, void* k_pool, void* v_pool, p
   p->head_scales = false;
   p->k = k_pool;
   p->v = v_pool;
-  p->maps_ready = false;
+  p->tile_maps_ready = false;
+  p->dec_maps_ready = false;
   *out = p;
   return PA_OK;
 }

@@ -132,8 +132,8 @@ __device__ __forceinline__ void mma_issue_stage(const AttnParams& p, MmaSmemHead
     const int t = a + k * BR;
     const int page = hdr->pid[(t >> lg_p) - j0];
     const int y = (page * p.Hkv + h) * P + (t & (P - 1));
-    tc::tma_load_2d(ks + k * BR * 128, &p.kmap, 0, y, &hdr->full[s]);
-    tc::tma_load_2d(vs + k * BR * 128, &p.vmap, 0, y, &hdr->full[s]);
+    tc::tma_load_2d(ks + k * BR * 128, &p.kmap_dec, 0, y, &hdr->full[s]);
+    tc::tma_load_2d(vs + k * BR * 128, &p.vmap_dec, 0, y, &hdr->full[s]);
   }
 }
 

@@ -103,6 +103,8 @@ struct AttnParams {
   CUtensorMap kmap;                       // bf16 K pool as [num_pages * Hkv * P][D], box 64 x P, 128B swizzle;
                                           // e4m3 pool (D = 128): bytes [num_pages * Hkv * P][128], box 128 x min(P, 32)
   CUtensorMap vmap;                       // V pool, same geometry
+  CUtensorMap kmap_dec;                   // D = 128 pools for the tensor-core decode units: bf16 boxes of
+  CUtensorMap vmap_dec;                   //   64 x min(P, 32), e4m3 boxes of 128 bytes x min(P, 32); 128B swizzle
 };
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
@@ -147,6 +149,12 @@ cudaError_t launch_decode_e4m3(const AttnParams& p, cudaStream_t stream);
 // [num_pages * Hkv * P][128], box 128 x min(P, 32), 128-byte swizzle.
 bool decode_e4m3_mma_eligible(int D, int G, bool q_bf16);
 cudaError_t launch_decode_e4m3_mma(const AttnParams& p, cudaStream_t stream);
+
+// Tensor-core decode units for bf16 pools, head_dim 128, bf16 queries, 3..8
+// query heads per kv head (p.kmap_dec / p.vmap_dec: bf16 boxes of 64 x
+// min(P, 32) rows).  The mixed launch runs the same units for its decode rows.
+bool decode_bf16_mma_eligible(int D, int G, bool q_bf16);
+cudaError_t launch_decode_bf16_mma(const AttnParams& p, cudaStream_t stream);
 
 // One launch whose first p.n_prefill_ctas CTAs run tensor-core prefill tiles
 // (bf16 q and K/V) and whose remaining CTAs run decode units.

@@ -4,8 +4,12 @@
 // running out of cache": decode rows of many sequences and a slice of a long
 // prompt share one launch).  A tile CTA has the decode CTA's shape (4 warps,
 // the same shared memory and register budget), so mixing costs the decode
-// units no occupancy.
+// units no occupancy.  The decode rows run the same units as in a decode-only
+// launch, so their bits do not depend on a chunk being present: the SIMT units
+// for G <= 2 or D = 64, the tensor-core units (on the CTA's first warp; the
+// others leave at once) for D = 128 and G >= 3.
 #include "pa_decode.cuh"
+#include "pa_decode_mma_bf16.cuh"
 #include "pa_prefill.cuh"
 
 namespace pa {
@@ -21,7 +25,11 @@ __global__ void __launch_bounds__(DecodeGeom<D, G, KV_BF16>::THREADS, DecodeGeom
     // a decode unit never allocates tensor memory: say so at once, or this CTA
     // would keep the SM's other CTA slots empty
     if (threadIdx.x < 32) tc::tmem_relinquish();
-    decode_unit<D, G, KV_BF16>(p, static_cast<int>(blockIdx.x) - p.n_prefill_ctas, smem);
+    if constexpr (D == 128 && G >= 3) {
+      if (threadIdx.x < 32) decode_unit_mma_bf16<G, 2>(p, static_cast<int>(blockIdx.x) - p.n_prefill_ctas, smem);
+    } else {
+      decode_unit<D, G, KV_BF16>(p, static_cast<int>(blockIdx.x) - p.n_prefill_ctas, smem);
+    }
   }
 }
 
@@ -31,7 +39,8 @@ cudaError_t launch_mixed_inst(const AttnParams& p0, cudaStream_t stream) {
   AttnParams p = p0;
   p.n_stages = Geo::STAGES;
   const size_t tile_smem = PrefillSmem<D>::BYTES;
-  const size_t dec_smem = decode_smem_for<D, G, KV_BF16>(p.P, Geo::STAGES);
+  const size_t dec_smem = (D == 128 && G >= 3) ? MmaBfGeom<G, 2>::SMEM
+                                               : decode_smem_for<D, G, KV_BF16>(p.P, Geo::STAGES);
   const size_t smem = tile_smem > dec_smem ? tile_smem : dec_smem;
   static int attr_bytes = 0;
   if (static_cast<int>(smem) > attr_bytes) {

@@ -87,3 +87,19 @@ def test_decode_rows_unchanged_beside_a_prefill_chunk():
     together = attend_rows(st, np.arange(wl.n_rows), chunks=wl.chunks)
     alone = attend_rows(st, dec)
     assert together[dec].tobytes() == alone.tobytes()
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(16, 4), (28, 4), (32, 4)])
+def test_decode_rows_unchanged_beside_a_chunk_on_tensor_core_units(Hq, Hkv):
+    """G >= 3 (bf16, D 128): decode rows run on the tensor-core units, inside
+    the mixed launch as in a decode-only launch; their bits must not change."""
+    wl = W.chunked_step(71 + Hq, chunks=[(200, 180, 416)], decode_ctx=[5, 64, 333, 700, 1029], Hq=Hq, Hkv=Hkv)
+    st = pa_setup.upload(wl)
+    st.append_step()
+    torch.cuda.synchronize()
+    dec = wl.decode_rows()
+    together = attend_rows(st, np.arange(wl.n_rows), chunks=wl.chunks)
+    alone = attend_rows(st, dec)
+    assert together[dec].tobytes() == alone.tobytes()
+    shuffled = np.random.default_rng(1).permutation(dec)
+    assert attend_rows(st, shuffled).tobytes() == together[shuffled].tobytes()
