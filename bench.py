@@ -269,6 +269,24 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The largest of every rank's x: the slowest replica sets the job's time.
+    `dist` is torch.distributed with an initialised process group, or None
+    for one process."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(rows_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: the rows every replica processed in one step over
+    the step time (already the maximum over ranks)."""
+    return rows_per_rank * world / (ms_per_step / 1e3)
+
+
 def attention_kernel_name(wl) -> str:
     """The kernel pa_attention launches for this workload's decode rows."""
     import workloads as W
@@ -367,13 +385,9 @@ def run_ours(args):
         att_ev[i][1].record(stream)
     torch.cuda.synchronize()
     att_ms = [a.elapsed_time(b) for a, b in att_ev]
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist if world > 1 else None, dev)
     ms_per_step = ms_total / args.steps
-    rows_total = wl.n_rows * world
-    value = rows_total / (ms_per_step / 1e3)
+    value = job_rows_per_s(wl.n_rows, world, ms_per_step)
 
     # ---- e2e: the same step through the public API with host buffers
     pin = lambda t: t.detach().cpu().pin_memory()
@@ -404,11 +418,8 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = rows_total / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e2e_ms, dist if world > 1 else None, dev)
+    e2e_value = job_rows_per_s(wl.n_rows, world, e2e_ms)
 
     # ---- roofline of the attention kernel
     alg_bytes = kv_unique + wl.qo_bytes()
