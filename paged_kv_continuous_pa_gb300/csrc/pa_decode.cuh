@@ -513,8 +513,8 @@ __device__ __forceinline__ void decode_finish(const AttnParams& p, bool bad, int
 template <int D, int G, int KVT>
 __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsigned char* smem) {
   using Geo = DecodeGeom<D, G, KVT>;
-  constexpr int NW = Geo::NW, LPT = Geo::LPT, TPS = Geo::TPS, U = Geo::U, NV = Geo::NV, EPV = Geo::EPV;
-  constexpr int PE = Geo::PE, PLT = Geo::PLT, TPV = Geo::TPV, NPV = Geo::NPV, RB = Geo::RB, WT = Geo::WT;
+  constexpr int NW = Geo::NW, LPT = Geo::LPT, NV = Geo::NV, EPV = Geo::EPV;
+  constexpr int PE = Geo::PE, PLT = Geo::PLT, RB = Geo::RB, WT = Geo::WT;
   constexpr int ST = kStageTokens;
 
   const int h = unit % p.Hkv;

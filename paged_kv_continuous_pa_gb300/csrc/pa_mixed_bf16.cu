@@ -18,7 +18,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(DecodeGeom<D, G, KV_BF16>::THREADS, DecodeGeom<D, G, KV_BF16>::MIN_CTAS)
     mixed_kernel(const __grid_constant__ AttnParams p) {
   static_assert(DecodeGeom<D, G, KV_BF16>::THREADS == kTileM, "a tile CTA has one thread per tile row");
-  extern __shared__ __align__(1024) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];  // the tile and tensor-core units align to 1024 by hand
   if (static_cast<int>(blockIdx.x) < p.n_prefill_ctas) {
     prefill_tile<D, G>(p, static_cast<int>(blockIdx.x), smem);
   } else {
