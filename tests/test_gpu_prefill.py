@@ -42,11 +42,13 @@ def test_head_dims_and_pages(D, P):
                   f"D{D} P{P}")
 
 
-def test_long_tile_key_ranges_split_and_merge():
+@pytest.mark.parametrize("P", [16, 32, 128, 256])
+def test_long_tile_key_ranges_split_and_merge(P):
     """A chunk far into its sequence: each tile's keys span several key ranges
-    that separate CTAs process and the last one merges in ascending order."""
-    wl = W.chunked_step(45, [(9000, 200, 9300)], decode_ctx=[50, 7000], Hq=8, Hkv=2)
-    run_and_check(wl, "chunk at 9000")
+    that separate CTAs process and the last one merges in ascending order (at
+    P = 16 a range's page-id table is at its largest, 256 pages)."""
+    wl = W.chunked_step(45, [(9000, 200, 9300)], decode_ctx=[50, 7000], Hq=8, Hkv=2, P=P)
+    run_and_check(wl, f"chunk at 9000, P{P}")
 
 
 def test_several_chunks_with_decode_rows():
