@@ -87,6 +87,23 @@ def test_page_sizes_and_dtypes(P, kv_dtype):
     assert_close(got, oracle_out(wl, kp, vp), wl, f"P{P} kv{kv_dtype}")
 
 
+@pytest.mark.parametrize("P", [16, 64, 128, 256])
+@pytest.mark.parametrize("G", [3, 7])
+def test_bf16_tensor_core_units_page_sizes(G, P):
+    """The bf16 tensor-core decode units (D 128, G 3..8): 32-token stages that are
+    two pages, one page or part of a page, contexts ending on and just past
+    stage and page boundaries."""
+    ctx = [1, 31, 32, 33, P - 1, P, P + 1, 2 * P + 5, 700]
+    wl = W._decode_workload("bfmma", 1300 + 11 * G + P, ctx, 2 * G, 2, 128, P, W.BF16, W.BF16, max_ctx=768,
+                            spare_pages=4, description="bf16 tensor-core units, page sizes")
+    st = run_step(wl)
+    assert int(st.status.item()) == 0
+    kp, vp = oracle_pools(wl)
+    check_pools(st, kp, vp)
+    got = W.bf16_bits_to_f32(pa_setup.to_numpy(st.out)).astype(np.float64)
+    assert_close(got, oracle_out(wl, kp, vp), wl, f"bf16 mma G{G} P{P}")
+
+
 @pytest.mark.parametrize("G", [1, 3, 5, 6, 8])
 @pytest.mark.parametrize("D", [64, 128])
 def test_group_sizes(G, D):
