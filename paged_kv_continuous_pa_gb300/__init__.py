@@ -153,6 +153,40 @@ def _ptr(t) -> Optional[int]:
     return t.data_ptr()
 
 
+def _check_index(t, name: str, n: Optional[int] = None, dims: int = 1):
+    """The int32 index arrays the kernels read: dtype and shape, before any pointer is taken."""
+    import torch
+    if t.dtype != torch.int32:
+        raise TypeError(f"{name} must be int32, got {t.dtype}")
+    if t.dim() != dims or (n is not None and int(t.shape[0]) != n):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}; expected {dims}-D" + (f" with {n} rows" if n is not None else ""))
+
+
+def _check_rows(pool: "Pool", q, seq_ids, positions, block_tables, out, status):
+    """q / out [n, Hq, D] with the pool's D; seq_ids / positions int32 [n]; block_tables int32 [num_seqs, max_blocks]."""
+    _check_index(seq_ids, "seq_ids")
+    n = int(seq_ids.shape[0])
+    _check_index(positions, "positions", n)
+    _check_index(block_tables, "block_tables", dims=2)
+    if status is not None:
+        _check_index(status, "status")
+    if q.dim() != 3 or int(q.shape[0]) != n or int(q.shape[2]) != pool.head_dim:
+        raise ValueError(f"q has shape {tuple(q.shape)}; expected [{n}, Hq, {pool.head_dim}]")
+    if out.dtype != q.dtype or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must match q's shape and dtype")
+    return n
+
+
+def _check_kv_rows(pool: "Pool", k_new, v_new, n: int):
+    """k_new / v_new [n, Hkv, D] with the pool's Hkv and D, one dtype."""
+    want = (n, pool.num_kv_heads, pool.head_dim)
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if tuple(t.shape) != want:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}; expected {list(want)}")
+    if k_new.dtype != v_new.dtype:
+        raise ValueError("k_new and v_new must share a dtype")
+
+
 def _stream(stream) -> Optional[int]:
     import torch
     if stream is None:
@@ -253,7 +287,13 @@ class Pages:
 
 def append_kv(pool: Pool, k_new, v_new, seq_ids, positions, block_tables, status=None, stream=None):
     """Scatter rows' new K/V ([n, Hkv, D], f32 or bf16) into their page slots (one launch)."""
+    _check_index(seq_ids, "seq_ids")
     n = int(seq_ids.shape[0])
+    _check_index(positions, "positions", n)
+    _check_index(block_tables, "block_tables", dims=2)
+    if status is not None:
+        _check_index(status, "status")
+    _check_kv_rows(pool, k_new, v_new, n)
     num_seqs, max_blocks = (int(x) for x in block_tables.shape)
     _check(load().pa_append_kv(pool.handle, n, _ptr(k_new), _ptr(v_new), _dtype_code(k_new), _ptr(seq_ids),
                                _ptr(positions), _ptr(block_tables), num_seqs, max_blocks, _ptr(status),
@@ -271,11 +311,9 @@ def attention(pool: Pool, q, seq_ids, positions, block_tables, out,
               chunks: Sequence[Tuple[int, int]] = (), softmax_scale: float = 0.0, workspace=None, status=None,
               stream=None):
     """Paged attention of every row (q [n, Hq, D] f32|bf16) into out (same shape and dtype)."""
-    n = int(seq_ids.shape[0])
+    n = _check_rows(pool, q, seq_ids, positions, block_tables, out, status)
     num_q_heads = int(q.shape[1])
     num_seqs, max_blocks = (int(x) for x in block_tables.shape)
-    if out.dtype != q.dtype or tuple(out.shape) != tuple(q.shape):
-        raise ValueError("out must match q's shape and dtype")
     arr = (Chunk * max(1, len(chunks)))(*[Chunk(int(b), int(c)) for b, c in chunks])
     ws_ptr = _ptr(workspace) if workspace is not None else None
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
@@ -288,13 +326,10 @@ def step(pool: Pool, q, k_new, v_new, seq_ids, positions, block_tables, out,
          chunks: Sequence[Tuple[int, int]] = (), softmax_scale: float = 0.0, workspace=None, status=None, stream=None):
     """append_kv() then attention() of the same rows as one call: the attention
     kernel starts while the append runs (bit-identical to the two calls)."""
-    n = int(seq_ids.shape[0])
+    n = _check_rows(pool, q, seq_ids, positions, block_tables, out, status)
+    _check_kv_rows(pool, k_new, v_new, n)
     num_q_heads = int(q.shape[1])
     num_seqs, max_blocks = (int(x) for x in block_tables.shape)
-    if out.dtype != q.dtype or tuple(out.shape) != tuple(q.shape):
-        raise ValueError("out must match q's shape and dtype")
-    if k_new.dtype != v_new.dtype:
-        raise ValueError("k_new and v_new must share a dtype")
     arr = (Chunk * max(1, len(chunks)))(*[Chunk(int(b), int(c)) for b, c in chunks])
     ws_ptr = _ptr(workspace) if workspace is not None else None
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
@@ -308,11 +343,9 @@ def attention_noalloc(pool: Pool, q, seq_ids, positions, block_tables, out,
                       chunks: Sequence[Tuple[int, int]] = (), softmax_scale: float = 0.0, status=None, stream=None):
     """attention() for callers that cannot allocate: split-KV scratch comes from
     a fixed 32 MiB array inside the library instead of a workspace tensor."""
-    n = int(seq_ids.shape[0])
+    n = _check_rows(pool, q, seq_ids, positions, block_tables, out, status)
     num_q_heads = int(q.shape[1])
     num_seqs, max_blocks = (int(x) for x in block_tables.shape)
-    if out.dtype != q.dtype or tuple(out.shape) != tuple(q.shape):
-        raise ValueError("out must match q's shape and dtype")
     arr = (Chunk * max(1, len(chunks)))(*[Chunk(int(b), int(c)) for b, c in chunks])
     _check(load().pa_attention_noalloc(pool.handle, n, _ptr(q), _dtype_code(q), num_q_heads, _ptr(seq_ids),
                                        _ptr(positions), _ptr(block_tables), num_seqs, max_blocks,
