@@ -212,6 +212,10 @@ pa_status pa_attention_noalloc(const pa_pool *pool, int32_t n_rows, const void *
 /* Split-KV chunk length in tokens: a row at position p is cut into
  * ceil((p + 1) / split) pieces merged in ascending order.  A process-wide
  * constant (default 4096), a multiple of 64 up to 4096, never derived from the batch.
+ * These settings (split length, wait limit, injected stall) may be changed from
+ * any thread; a call reads each of them once, when it starts, so one call never
+ * mixes two values.  A workspace sized by pa_attention_workspace_bytes before a
+ * change may be too small after it: the call then returns PA_ERR_INVALID_ARG.
  * Changing it changes output bits (within tolerance) for rows longer than it.
  * Returns PA_ERR_INVALID_ARG for a value that is not a positive multiple of 64. */
 pa_status pa_set_split_tokens(int32_t tokens);

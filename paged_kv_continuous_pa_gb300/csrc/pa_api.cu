@@ -37,9 +37,10 @@ void pa::count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 namespace {
 
 thread_local char g_last_error[512] = "";
-int32_t g_split_tokens = pa::kDefaultSplitTokens;
-uint32_t g_wait_limit = pa::kDefaultWaitLimit;
-int32_t g_debug_stall = 0;
+// process-wide settings; any thread may change them, and a call reads each once
+std::atomic<int32_t> g_split_tokens{pa::kDefaultSplitTokens};
+std::atomic<uint32_t> g_wait_limit{pa::kDefaultWaitLimit};
+std::atomic<int32_t> g_debug_stall{0};
 
 pa_status fail(pa_status st, const char* fmt, ...) {
   va_list ap;
@@ -57,9 +58,9 @@ size_t elt_bytes(pa_dtype t) { return t == PA_F32 ? 4 : t == PA_BF16 ? 2 : 1; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int max_splits_for(const pa_pool_desc& d, int32_t max_blocks) {
+int max_splits_for(const pa_pool_desc& d, int32_t max_blocks, int32_t split_tokens) {
   const long long cap = static_cast<long long>(max_blocks) * d.page_size;
-  return static_cast<int>((cap + g_split_tokens - 1) / g_split_tokens);
+  return static_cast<int>((cap + split_tokens - 1) / split_tokens);
 }
 
 // How one pa_attention call is laid out: which chunks take the tensor-core
@@ -80,10 +81,10 @@ struct Plan {
 };
 
 Plan make_plan(const pa_pool_desc& d, int32_t n_rows, int32_t hq, int32_t max_blocks, const pa_chunk* chunks,
-               int32_t n_chunks, bool tile_dtypes) {
+               int32_t n_chunks, bool tile_dtypes, int32_t split_tokens) {
   Plan pl;
   pl.G = hq / d.num_kv_heads;
-  pl.max_splits = max_splits_for(d, max_blocks);
+  pl.max_splits = max_splits_for(d, max_blocks, split_tokens);
   pl.R = pa::kTileRowsTotal / pl.G;
   if (tile_dtypes && chunks != nullptr) {
     const long long keys = static_cast<long long>(max_blocks) * d.page_size;
@@ -303,8 +304,9 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
   if (!q || !seq_ids || !positions || !block_tables || !out)
     return fail(PA_ERR_INVALID_ARG, "attention: a device pointer is NULL");
   if (!aligned(q, 16) || !aligned(out, 16)) return fail(PA_ERR_INVALID_ARG, "q / out must be 16-byte aligned");
+  const int32_t split_tokens = g_split_tokens.load(std::memory_order_relaxed);  // one value for the plan and the kernels
   const Plan pl = make_plan(d, n_rows, num_q_heads, max_blocks_per_seq, chunks, n_chunks,
-                            q_dtype == PA_BF16 && d.kv_dtype == PA_BF16);
+                            q_dtype == PA_BF16 && d.kv_dtype == PA_BF16, split_tokens);
   if (pl.total > 0) {
     if (workspace == nullptr || workspace_bytes < pl.total)
       return fail(PA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", pl.total,
@@ -330,7 +332,7 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
   p.Hkv = d.num_kv_heads;
   p.D = d.head_dim;
   p.q_is_bf16 = q_dtype == PA_BF16;
-  p.split_tokens = g_split_tokens;
+  p.split_tokens = split_tokens;
   p.max_splits = pl.max_splits;
   // per kv head (or entry 0 for all): softmax scale * k scale * log2(e), and the v scale
   p.head_scales = pool->head_scales ? 1 : 0;
@@ -354,8 +356,8 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
     }
   }
   p.status = status_dev;
-  p.wait_limit = g_wait_limit;
-  p.debug_stall = g_debug_stall;
+  p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  p.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
   p.n_prefill_ctas = 0;
   p.n_chunks = 0;
   p.sm_scale_log2 = static_cast<float>(sm * 1.4426950408889634073599246810018921);
@@ -496,7 +498,7 @@ size_t pa_attention_workspace_bytes(const pa_pool* pool, int32_t n_rows, int32_t
     return 0;
   // chunks of a bf16 pool may take the tile path (with bf16 queries): size for it
   return make_plan(pool->desc, n_rows, num_q_heads, max_blocks_per_seq, chunks, n_chunks,
-                   pool->desc.kv_dtype == PA_BF16)
+                   pool->desc.kv_dtype == PA_BF16, g_split_tokens.load(std::memory_order_relaxed))
       .total;
 }
 
@@ -528,15 +530,17 @@ pa_status pa_step(const pa_pool* pool, int32_t n_rows, const void* q, pa_dtype q
 pa_status pa_set_split_tokens(int32_t tokens) {
   if (tokens <= 0 || tokens % 64 != 0 || tokens > pa::kMaxSplitTokens)
     return fail(PA_ERR_INVALID_ARG, "split tokens %d is not a multiple of 64 in [64, %d]", tokens, pa::kMaxSplitTokens);
-  g_split_tokens = tokens;
+  g_split_tokens.store(tokens, std::memory_order_relaxed);
   return PA_OK;
 }
 
-int32_t pa_get_split_tokens(void) { return g_split_tokens; }
+int32_t pa_get_split_tokens(void) { return g_split_tokens.load(std::memory_order_relaxed); }
 
-void pa_set_wait_limit(uint32_t microseconds) { g_wait_limit = microseconds == 0 ? pa::kDefaultWaitLimit : microseconds; }
+void pa_set_wait_limit(uint32_t microseconds) {
+  g_wait_limit.store(microseconds == 0 ? pa::kDefaultWaitLimit : microseconds, std::memory_order_relaxed);
+}
 
-void pa_debug_stall_waits(int32_t enable) { g_debug_stall = enable != 0; }
+void pa_debug_stall_waits(int32_t enable) { g_debug_stall.store(enable != 0, std::memory_order_relaxed); }
 
 const char* pa_status_string(pa_status status) {
   switch (status) {

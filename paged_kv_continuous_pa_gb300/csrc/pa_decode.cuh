@@ -721,13 +721,9 @@ cudaError_t launch_decode_inst(const AttnParams& p0, cudaStream_t stream) {
   AttnParams p = p0;
   p.n_stages = Geo::STAGES;
   const size_t smem = decode_smem_for<D, G, KVT>(p.P, p.n_stages);
-  static int attr_bytes = 0;  // largest dynamic shared memory size already allowed
-  if (static_cast<int>(smem) > attr_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G, KVT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_bytes = static_cast<int>(smem);
-  }
+  static std::atomic<unsigned long long> smem_done{0};  // devices on which the size is allowed
+  const cudaError_t ea = allow_dynamic_smem(decode_kernel<D, G, KVT>, smem_done, smem);
+  if (ea != cudaSuccess) return ea;
   const long long units = static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
   if (units <= 0) return cudaSuccess;
   const cudaError_t e = launch_kernel(decode_kernel<D, G, KVT>, dim3(static_cast<unsigned>(units)), dim3(Geo::THREADS),

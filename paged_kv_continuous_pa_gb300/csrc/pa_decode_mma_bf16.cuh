@@ -347,16 +347,18 @@ __global__ void __launch_bounds__(32, 8) decode_mma_bf16_kernel(const __grid_con
   decode_unit_mma_bf16<G, NST>(p, static_cast<int>(blockIdx.x), smem);
 }
 
+// Devices on which decode_mma_bf16_kernel<G, NST> may use its dynamic shared memory.
+template <int G, int NST>
+std::atomic<unsigned long long>& mma_bf16_smem_done() {
+  static std::atomic<unsigned long long> done{0};
+  return done;
+}
+
 template <int G, int NST>
 cudaError_t launch_decode_mma_bf16_nst(const AttnParams& p, cudaStream_t stream, unsigned units) {
   using Geo = MmaBfGeom<G, NST>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_bf16_kernel<G, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Geo::SMEM));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t ea = allow_dynamic_smem(decode_mma_bf16_kernel<G, NST>, mma_bf16_smem_done<G, NST>(), Geo::SMEM);
+  if (ea != cudaSuccess) return ea;
   const cudaError_t e = launch_kernel(decode_mma_bf16_kernel<G, NST>, dim3(units), dim3(Geo::THREADS), Geo::SMEM,
                                       stream, p.dependent != 0, p);
   count_launch();
@@ -365,18 +367,9 @@ cudaError_t launch_decode_mma_bf16_nst(const AttnParams& p, cudaStream_t stream,
 
 template <int G, int NST>
 long long mma_bf16_resident_units() {
-  static long long cap = -1;
-  if (cap < 0) {
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(decode_mma_bf16_kernel<G, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(MmaBfGeom<G, NST>::SMEM)) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_bf16_kernel<G, NST>, 32,
-                                                      MmaBfGeom<G, NST>::SMEM) != cudaSuccess)
-      return 0;
-    cap = static_cast<long long>(sms) * per_sm;
-  }
-  return cap;
+  static std::atomic<long long> cache[64];  // per device: resident CTAs + 1, 0 until known
+  return resident_ctas(decode_mma_bf16_kernel<G, NST>, cache, mma_bf16_smem_done<G, NST>(), 32,
+                       MmaBfGeom<G, NST>::SMEM);
 }
 
 #ifndef PA_MMA_BF16_NST

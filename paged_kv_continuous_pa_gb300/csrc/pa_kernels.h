@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace pa {
 
 constexpr int kMaxChunks = 16;          // prefill chunks per pa_attention call
@@ -108,6 +110,44 @@ struct AttnParams {
 };
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+
+// Let `kernel` use `bytes` of dynamic shared memory on the current device.
+// The attribute is per device, so it is set once for each device this process
+// launches on (`done`: one bit per device, kept by the caller per kernel).
+// Every thread sets the same value, so concurrent first calls are harmless.
+template <typename Kernel>
+cudaError_t allow_dynamic_smem(Kernel kernel, std::atomic<unsigned long long>& done, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
+// CTAs of `kernel` (`threads` threads, `bytes` of dynamic shared memory)
+// resident on the current device at once, computed once per device (`cache`:
+// value + 1 per device, 0 until known).  0 if it cannot be queried.
+template <typename Kernel>
+long long resident_ctas(Kernel kernel, std::atomic<long long> (&cache)[64], std::atomic<unsigned long long>& smem_done,
+                        int threads, size_t bytes) {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64) {
+    const long long c = cache[dev].load(std::memory_order_acquire);
+    if (c > 0) return c - 1;
+  }
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      allow_dynamic_smem(kernel, smem_done, bytes) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, bytes) != cudaSuccess)
+    return 0;
+  const long long cap = static_cast<long long>(sms) * per_sm;
+  if (dev < 64) cache[dev].store(cap + 1, std::memory_order_release);
+  return cap;
+}
+
 
 // Launch `kernel` normally, or (dependent) as a programmatic dependent of the
 // previous kernel in the stream: it may start while that kernel runs and must

@@ -42,13 +42,9 @@ cudaError_t launch_mixed_inst(const AttnParams& p0, cudaStream_t stream) {
   const size_t dec_smem = (D == 128 && G >= 3) ? MmaBfGeom<G, 2>::SMEM
                                                : decode_smem_for<D, G, KV_BF16>(p.P, Geo::STAGES);
   const size_t smem = tile_smem > dec_smem ? tile_smem : dec_smem;
-  static int attr_bytes = 0;
-  if (static_cast<int>(smem) > attr_bytes) {
-    cudaError_t e =
-        cudaFuncSetAttribute(mixed_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_bytes = static_cast<int>(smem);
-  }
+  static std::atomic<unsigned long long> smem_done{0};  // devices on which the size is allowed
+  const cudaError_t ea = allow_dynamic_smem(mixed_kernel<D, G>, smem_done, smem);
+  if (ea != cudaSuccess) return ea;
   const long long ctas = static_cast<long long>(p.n_prefill_ctas) + static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
   if (ctas <= 0) return cudaSuccess;
   const cudaError_t e = launch_kernel(mixed_kernel<D, G>, dim3(static_cast<unsigned>(ctas)), dim3(Geo::THREADS), smem,

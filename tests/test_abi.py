@@ -131,6 +131,48 @@ def test_split_tokens_setting(lib):
         lib.pa_set_split_tokens(old)
 
 
+def test_settings_change_from_other_threads(lib):
+    """One thread flips the split length while others size workspaces: every
+    answer is the one of the two settings, never a mix (a call reads it once)."""
+    import threading
+    st, h = _create(lib, _desc())
+    assert st == pa.PA_OK
+    old = lib.pa_get_split_tokens()
+    try:
+        sizes = {}
+        for t in (1024, 4096):
+            assert lib.pa_set_split_tokens(t) == pa.PA_OK
+            sizes[t] = lib.pa_attention_workspace_bytes(h, 64, 8, 200, None, 0)
+        assert sizes[1024] > sizes[4096] > 0
+        stop = threading.Event()
+        seen, bad = set(), []
+
+        def flip():
+            i = 0
+            while not stop.is_set():
+                lib.pa_set_split_tokens((1024, 4096)[i % 2])
+                i += 1
+
+        def size():
+            for _ in range(20000):
+                v = lib.pa_attention_workspace_bytes(h, 64, 8, 200, None, 0)
+                seen.add(v)
+                if v not in sizes.values():
+                    bad.append(v)
+
+        threads = [threading.Thread(target=flip)] + [threading.Thread(target=size) for _ in range(3)]
+        for t in threads:
+            t.start()
+        for t in threads[1:]:
+            t.join()
+        stop.set()
+        threads[0].join()
+        assert not bad and seen <= set(sizes.values())
+    finally:
+        lib.pa_set_split_tokens(old)
+        lib.pa_pool_destroy(h)
+
+
 def test_head_scales_validation(lib):
     arr = lambda *v: (ctypes.c_float * len(v))(*v)
     st, h = _create(lib, _desc(kv_dtype=pa.PA_FP8_E4M3, k_scale=0.5, v_scale=0.5))
