@@ -62,3 +62,29 @@ def test_equal_head_scales_give_per_tensor_bits():
         assert int(st.status.item()) == 0
         outs.append((st.k_pool.view(torch.uint8).clone(), st.out.view(torch.int16).clone()))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_sixty_four_kv_heads_each_with_its_scale(D):
+    """The largest per-head table (64 kv heads, one query head each): every head's
+    scale is its own, on the tensor-core units (D 128) and the SIMT units (D 64).
+    The values keep unit scale (the tolerance's absolute part is stated for
+    those); the scales differ by head, from amax / 448 up to 4.5 times that, so
+    a head read with another head's scale is off by their ratio."""
+    Hkv = 64
+    wl = W._decode_workload("hs64", 70 + D, [1, 31, 33, 64, 300], Hkv, Hkv, D, 32, W.E4M3, W.BF16, max_ctx=320,
+                            spare_pages=4, description="64 per-head fp8 scales")
+    f = (1.0 + 0.5 * (np.arange(Hkv) % 8)).astype(np.float32)
+    amax_k = max(np.abs(W.as_f32(wl.hist_k, wl.in_dtype)).max(), np.abs(W.as_f32(wl.k_new, wl.in_dtype)).max())
+    amax_v = max(np.abs(W.as_f32(wl.hist_v, wl.in_dtype)).max(), np.abs(W.as_f32(wl.v_new, wl.in_dtype)).max())
+    wl.k_scale = (np.float32(amax_k) / np.float32(448.0) * f).astype(np.float32)
+    wl.v_scale = (np.float32(amax_v) / np.float32(448.0) * f).astype(np.float32)
+    st = pa_setup.upload(wl)
+    st.step()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    kp, vp = oracle_pools(wl)
+    assert pa_setup.to_numpy(st.k_pool).tobytes() == kp.tobytes()
+    assert pa_setup.to_numpy(st.v_pool).tobytes() == vp.tobytes()
+    got = W.bf16_bits_to_f32(pa_setup.to_numpy(st.out)).astype(np.float64)
+    assert_close(got, oracle_out(wl, kp, vp), wl, f"64 heads D{D}")

@@ -51,6 +51,17 @@ def test_long_tile_key_ranges_split_and_merge(P):
     run_and_check(wl, f"chunk at 9000, P{P}")
 
 
+def test_sixteen_chunks_the_most_one_call_takes():
+    """16 chunks in one launch (the limit), tile-path and decode-path chunks
+    (one shorter than a tile's 16 rows) beside decode rows."""
+    chunks = []
+    for i in range(16):
+        n = 5 if i == 6 else 16 + (i % 3) * 9
+        start = 11 * i
+        chunks.append((start, n, start + n + 7))
+    run_and_check(W.chunked_step(61, chunks, decode_ctx=[3, 200, 650], Hq=8, Hkv=2), "16 chunks")
+
+
 def test_several_chunks_with_decode_rows():
     wl = W.chunked_step(41, [(0, 40, 40), (200, 77, 300), (513, 128, 700)], decode_ctx=[1, 64, 999, 2000])
     run_and_check(wl, "three chunks + decode rows")
