@@ -23,7 +23,7 @@
  *     granularity open; the oracle takes a per-tensor scale, or one scale per
  *     KV head.
  *
- * Readings where the pages are silent (each listed in the design doc):
+ * Readings where the pages are silent:
  *   - a row at position p attends keys 0..p inclusive (causal, own token included);
  *   - q head g reads kv head g / (Hq / Hkv);
  *   - fp8 is OCP E4M3 (bias 7, max finite 448, no infinities, S.1111.111 is NaN),
