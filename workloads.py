@@ -6,13 +6,15 @@ of the attention arithmetic (no append, no softmax, no fp8 encoding: the fp8
 scale below is the harness's calibration choice, handed unchanged to both
 sides).  bf16 arrays are numpy ``uint16`` bit patterns, fp8 pools ``uint8``.
 
-The shapes follow the workloads of the pages (see the design doc for the recipe):
+The shapes follow the workloads of the pages; the pages' own prompts and
+evaluation queries are private, so these inputs stand in for their shapes only:
   tiny decode         4 sequences, contexts {5,33,64,100}, Hq 8 / Hkv 2, D 64, fp32, P 32, 16 pages
   batched decode      512 sequences, contexts U{64..2662}, Hq 16 / Hkv 8, D 128, bf16, P 32
   mixed step          256 decode rows (U{64..1024}) + a 256-row causal chunk at 1024 of a 2662-token prompt
   shared prefix       768 sequences, Hq 28 / Hkv 4, D 128, fp8 e4m3 K/V, bf16 Q, 128 + U{0..127} tokens,
                       70% sharing a 90-token prefix (its two full 32-token pages shared)
   long context        64 sequences x 32768 tokens, Hq 32 / Hkv 8, D 128, bf16, P 16, split-KV
+  fp8 variants        the batched-decode and long-context shapes with e4m3 pools (per-tensor scales)
 """
 from __future__ import annotations
 
