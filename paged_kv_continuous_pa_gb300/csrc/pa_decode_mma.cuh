@@ -30,9 +30,15 @@
 //     row loads with byte permutes and e4m3x2 -> f16x2 conversions; thread t
 //     owns head elements 16 (t/4) .. 16 (t/4) + 15, so the MMA's m rows are a
 //     fixed permutation of the head dim, undone when the accumulators are
-//     written out.  B = P^T: the softmax weights, rounded to f16 (weights are
-//     <= 2^8 by the lazy reference max), moved into fragment order with
-//     movmatrix.trans.
+//     written out.  B = P^T: each softmax weight w (<= 2^8 by the lazy
+//     reference max) as two f16 parts, hi = f16(w) and lo = f16(w - hi), moved
+//     into fragment order with movmatrix.trans; two MMAs per k-step, so the
+//     product sees w to about 2^-22 relative (f16 alone would leave 2^-11,
+//     an error that grows with the values' magnitude).  With G <= 4 the hi
+//     and lo parts share one MMA: columns 4..7 repeat query heads 0..3, so
+//     their scores, references and weights are the same, and they carry the
+//     lo parts into accumulator columns of their own, added to the hi
+//     columns once at the end of the unit.
 //   * The query enters as f16, scaled by a power of two chosen per (row, kv
 //     head) so that its largest element is below 2^15; the power is folded
 //     back into the score scale.  bf16 values in the f16 normal range are exact.
@@ -152,13 +158,17 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
   const int g4 = lane >> 2;  // fragment group: key row (QK), head element block (PV), query head (B operand)
   const int t4 = lane & 3;   // thread in group
   const size_t out_row = static_cast<size_t>(row) * p.Hq + static_cast<size_t>(h) * G;
+  // G <= 4: MMA column n >= 4 repeats query head n - 4 and carries the lo
+  // parts of its weights (the hi and lo products in one MMA)
+  constexpr bool PACK = G <= 4;
+  const int qhead = g4 < G ? g4 : ((PACK && g4 >= 4 && g4 - 4 < G) ? g4 - 4 : -1);  // -1: a zero column
   // The query words this lane needs (bf16), loaded first so that their latency
   // overlaps the sequence and page-id lookups: head g4 of the group (head 0
   // stands in for heads >= G), elements 32kb + 4 t4 .. +3 and 32kb + 16 + 4 t4 .. +3.
   uint2 qraw[4][2];
   {
     const uint2* qs = reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.q) +
-                                                     (out_row + (g4 < G ? g4 : 0)) * D);
+                                                     (out_row + (qhead >= 0 ? qhead : 0)) * D);
 #pragma unroll
     for (int kb = 0; kb < 4; ++kb) {
       qraw[kb][0] = __ldg(qs + 8 * kb + t4);
@@ -228,7 +238,7 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
   {
     float qv[4][8];
     float amax = 0.0f;
-    const bool head_ok = g4 < G;
+    const bool head_ok = qhead >= 0;
 #pragma unroll
     for (int kb = 0; kb < 4; ++kb) {
       const uint2 w0 = qraw[kb][0], w1 = qraw[kb][1];
@@ -260,9 +270,9 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
 
   // ---- softmax state: heads 2 t4 and 2 t4 + 1; O^T rows d(i, g4) = 16 g4 + i and
   // d(i, g4 + 8) = 16 g4 + 8 + i for m-tile i.  The sums of the weights come
-  // from one more MMA per 16 keys with an all-ones A: lsum[0] / lsum[1] hold
+  // from two more MMAs per 16 keys with an all-ones A: lsum[0] / lsum[1] hold
   // heads 2 t4 / 2 t4 + 1 (lsum[2..3] repeat them), summed from the same
-  // f16-rounded weights that meet V.
+  // (hi, lo) f16 parts of the weights that meet V.
   float m_ref[2] = {-INFINITY, -INFINITY};
   float o[8][4], lsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
@@ -354,14 +364,28 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
 #pragma unroll
         for (int c = 0; c < 4; ++c) t[mi][c] = fmaf(sc[mi][c], score_scale, -m_ref[c & 1]);
     }
-    // weights (masked keys: 2^-inf = 0), to f16 and into B-fragment order:
+    // weights w = 2^t (masked keys: 2^-inf = 0) as hi = f16(w), lo = f16(w - hi),
+    // into B-fragment order:
     // C layout (key g4 / g4+8, heads 2t4, 2t4+1) -> B layout (head g4, keys 2t4, 2t4+1)
-    uint32_t pb[2][2];  // P^T fragments: [k-step][keys 0..7 / 8..15 of it]
+    uint32_t phi[2][2], plo[2][2];  // P^T fragments: [k-step][keys 0..7 / 8..15 of it]
 #pragma unroll
     for (int mi = 0; mi < 2; ++mi) {
-      pb[mi][0] = movmatrix_trans(pack_f16x2(ex2(t[mi][0]), ex2(t[mi][1])));
-      pb[mi][1] = movmatrix_trans(pack_f16x2(ex2(t[mi][2]), ex2(t[mi][3])));
-      mma_f16_16816(lsum, ones, pb[mi][0], pb[mi][1]);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const float w0 = ex2(t[mi][2 * half]), w1 = ex2(t[mi][2 * half + 1]);
+        const __half2 hi = __floats2half2_rn(w0, w1);
+        const float2 hf = __half22float2(hi);
+        const uint32_t hi_w = *reinterpret_cast<const uint32_t*>(&hi);
+        const uint32_t lo_w = pack_f16x2(__fsub_rn(w0, hf.x), __fsub_rn(w1, hf.y));
+        if constexpr (PACK) {
+          phi[mi][half] = movmatrix_trans(t4 < 2 ? hi_w : lo_w);  // columns 0..3 hi, 4..7 lo
+        } else {
+          phi[mi][half] = movmatrix_trans(hi_w);
+          plo[mi][half] = movmatrix_trans(lo_w);
+        }
+      }
+      mma_f16_16816(lsum, ones, phi[mi][0], phi[mi][1]);
+      if constexpr (!PACK) mma_f16_16816(lsum, ones, plo[mi][0], plo[mi][1]);
     }
     // ---- value rows past the row's position: zero them before they meet weight 0
     if (!full) {
@@ -395,10 +419,16 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
                                   e4m3x2_to_f16x2(cd_hi, true), e4m3x2_to_f16x2(cd8_hi, true)};
         const uint32_t a_j3[4] = {e4m3x2_to_f16x2(ab_hi, false), e4m3x2_to_f16x2(ab8_hi, false),
                                   e4m3x2_to_f16x2(cd_hi, false), e4m3x2_to_f16x2(cd8_hi, false)};
-        mma_f16_16816(o[4 * w + 0], a_j0, pb[mi][0], pb[mi][1]);
-        mma_f16_16816(o[4 * w + 1], a_j1, pb[mi][0], pb[mi][1]);
-        mma_f16_16816(o[4 * w + 2], a_j2, pb[mi][0], pb[mi][1]);
-        mma_f16_16816(o[4 * w + 3], a_j3, pb[mi][0], pb[mi][1]);
+        mma_f16_16816(o[4 * w + 0], a_j0, phi[mi][0], phi[mi][1]);
+        mma_f16_16816(o[4 * w + 1], a_j1, phi[mi][0], phi[mi][1]);
+        mma_f16_16816(o[4 * w + 2], a_j2, phi[mi][0], phi[mi][1]);
+        mma_f16_16816(o[4 * w + 3], a_j3, phi[mi][0], phi[mi][1]);
+        if constexpr (!PACK) {
+          mma_f16_16816(o[4 * w + 0], a_j0, plo[mi][0], plo[mi][1]);
+          mma_f16_16816(o[4 * w + 1], a_j1, plo[mi][0], plo[mi][1]);
+          mma_f16_16816(o[4 * w + 2], a_j2, plo[mi][0], plo[mi][1]);
+          mma_f16_16816(o[4 * w + 3], a_j3, plo[mi][0], plo[mi][1]);
+        }
       }
     }
     // ---- release the slot and refill it
@@ -416,6 +446,22 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
   }
   __syncwarp();
   const bool bad = hdr->bad != 0;
+  if constexpr (PACK) {
+    // add each head's lo columns (lane ^ 2) to its hi columns; their
+    // references are the same (equal scores), so the factor is 1 -- it is
+    // applied anyway so that the sum never mixes two references
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float m_lo = __shfl_xor_sync(0xffffffffu, m_ref[hh], 2);
+      const float f = m_lo == m_ref[hh] ? 1.0f : ex2(__fsub_rn(m_lo, m_ref[hh]));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        o[i][hh] = fmaf(__shfl_xor_sync(0xffffffffu, o[i][hh], 2), f, o[i][hh]);
+        o[i][2 + hh] = fmaf(__shfl_xor_sync(0xffffffffu, o[i][2 + hh], 2), f, o[i][2 + hh]);
+      }
+      lsum[hh] = fmaf(__shfl_xor_sync(0xffffffffu, lsum[hh], 2), f, lsum[hh]);
+    }
+  }
 
   if (nsplit == 1) {
     // ---- straight from the fragments: out = o * (v_scale / l), 16 bytes a store

@@ -137,3 +137,44 @@ def test_bad_page_and_stall_reported():
     torch.cuda.synchronize()
     assert int(st.status.item()) == 0
     assert torch.equal(out.view(torch.int16), good.view(torch.int16))
+
+
+def value_scaled(wl, k, per_head=False):
+    """K and V multiplied by 2^k (exact in bf16) with the fp8 scales calibrated
+    on the scaled values (amax / 448, per tensor or per kv head) and the
+    softmax scale divided by 2^k: the stored codes and the scores do not
+    change, every output grows by 2^k, and so does any error the P.V product
+    makes relative to the values."""
+    f = np.float32(2.0 ** k)
+    for name in ("hist_k", "hist_v", "k_new", "v_new"):
+        setattr(wl, name, W._cast(W.as_f32(getattr(wl, name), wl.in_dtype) * f, wl.in_dtype))
+    wl.softmax_scale = float(2.0 ** (-k)) / np.sqrt(128.0)
+    if not per_head:
+        return W._with_fp8_scales(wl)
+    ax = (0, 2)
+    amax_k = np.maximum(np.abs(W.as_f32(wl.hist_k, wl.in_dtype)).max(axis=ax),
+                        np.abs(W.as_f32(wl.k_new, wl.in_dtype)).max(axis=ax))
+    amax_v = np.maximum(np.abs(W.as_f32(wl.hist_v, wl.in_dtype)).max(axis=ax),
+                        np.abs(W.as_f32(wl.v_new, wl.in_dtype)).max(axis=ax))
+    wl.k_scale = (amax_k.astype(np.float32) / np.float32(448.0)).astype(np.float32)
+    wl.v_scale = (amax_v.astype(np.float32) / np.float32(448.0)).astype(np.float32)
+    return wl
+
+
+@pytest.mark.parametrize("k", [3, 6, 7])
+@pytest.mark.parametrize("P", [16, 32, 64])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_values_far_from_unit_scale(G, P, k):
+    """The P.V product must see each softmax weight to far better than f16's
+    2^-11: its error grows with the values' magnitude, and at 2^6..2^7 an
+    output that cancels to near zero would miss the absolute tolerance."""
+    wl = value_scaled(fp8_workload(700 + 10 * G + P + k, G, P), k)
+    check(wl, f"G{G} P{P} values x 2^{k}")
+
+
+@pytest.mark.parametrize("G", [1, 4, 7, 8])
+def test_values_far_from_unit_scale_per_head_scales(G):
+    """The same with one fp8 scale per kv head (4 kv heads, each calibrated on
+    its own values), values x 2^7."""
+    wl = value_scaled(fp8_workload(800 + G, G, 32, Hkv=4), 7, per_head=True)
+    check(wl, f"G{G} per-head scales, values x 2^7")
