@@ -15,6 +15,12 @@ host->device and the output copied back inside the timed region; `roofline`
 is the attention kernel's algorithmic bytes (valid K/V slots, shared pages
 once, plus Q and O) per launch over its CUDA-event time, against the measured
 HBM copy bandwidth.  `cpu_baseline` times the CPU oracle on the host cores.
+At N = 1 the default line also carries `workloads`: every config (tiny
+decode, batched decode, mixed step with its prefill tiles run alone, shared
+prefix, long context, both fp8 variants) timed the same way in the same
+process, each with its step and attention times, its HBM fractions (the
+attention launch alone, and the whole step with the append's bytes) and its
+own clock record.  --no-workloads skips them.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload batched_decode|mixed_step|shared_prefix|long_context|tiny_decode|
@@ -40,6 +46,9 @@ METRIC = "paged-attention rows/s and KV-read GB/s vs GB300 HBM roofline (1 GPU)"
 L2_BYTES = 129 * 1000 * 1000  # GB300 L2
 W_CONFIG_NAMES = ("batched_decode", "mixed_step", "shared_prefix", "long_context", "tiny_decode",
                   "batched_decode_fp8", "long_context_fp8")
+# the per-config entries of the default line, in the order they are timed
+ALL_WORKLOADS = ("tiny_decode", "batched_decode", "mixed_step", "shared_prefix", "long_context",
+                 "batched_decode_fp8", "long_context_fp8")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0  # burst
 
@@ -208,8 +217,7 @@ class OracleLeg:
     def __init__(self, wl, target_s: float = 3.0):
         import numpy as np
         import oracle
-        sys.path.insert(0, os.path.join(ROOT, "tests"))
-        from ref import oracle_pools  # test-side oracle setup
+        oracle_pools = oracle.workload_pools
 
         self.wl, self.oracle, self.np = wl, oracle, np
         self.cores = oracle.host_cores()
@@ -300,8 +308,122 @@ def attention_kernel_name(wl) -> str:
     return "decode_kernel"
 
 
+class Env:
+    """The device, stream and library handles one benchmark process uses."""
+
+    def __init__(self, torch, pa, W, pa_setup, dist, dev, world, rank):
+        self.torch, self.pa, self.W, self.pa_setup, self.dist = torch, pa, W, pa_setup, dist
+        self.dev, self.world, self.rank = dev, world, rank
+        self.stream = torch.cuda.current_stream()
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max_over_ranks(self, x):
+        return max_over_ranks(x, self.dist if self.world > 1 else None, self.dev)
+
+
+def time_steps(env, st, wl, steps: int, warmup: int):
+    """Warm up, then time `steps` pa_step calls (append + attention) and as many
+    attention launches alone, each bracketed by CUDA events on the launching
+    stream.  A step whose distinct K/V fits a few times in L2 is timed alone
+    after an L2 flush (write a buffer twice the L2, which evicts everything,
+    then read another one, so the evicted dirty lines are written back before
+    the step and not inside it); larger steps run back to back.  Returns a
+    dict of times plus the clock record and the library's launch count over
+    the timed steps."""
+    torch, pa = env.torch, env.pa
+    stream = env.stream
+    for _ in range(warmup):
+        st.step()
+    torch.cuda.synchronize()
+    st.status.zero_()
+    kv_unique = wl.kv_bytes_unique()
+    flush = kv_unique <= 4 * L2_BYTES
+    if flush:
+        fl_w = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=env.dev)
+        fl_r = torch.ones(2 * L2_BYTES // 4, dtype=torch.int32, device=env.dev)
+
+    def flush_l2():
+        fl_w.fill_(1)
+        fl_r.max()
+
+    ev_start, ev_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    launches0 = pa.kernel_launches()
+    with ClockSampler(env.dev.index) as clk:
+        env.barrier()
+        torch.cuda.synchronize()
+        ev_start.record(stream)
+        for i in range(steps):
+            if flush:
+                flush_l2()
+            step_ev[i][0].record(stream)
+            st.step()
+            step_ev[i][1].record(stream)
+        ev_end.record(stream)
+        torch.cuda.synchronize()
+        env.barrier()
+    launches = pa.kernel_launches() - launches0
+    status = int(st.status.item())
+    if status != 0:
+        raise RuntimeError(f"device status {status} ({pa.status_string(status)}) during the timed steps of {wl.name}")
+    # the steps' own device time (the flushes between them excluded)
+    ms_total = sum(a.elapsed_time(b) for a, b in step_ev) if flush else ev_start.elapsed_time(ev_end)
+
+    att_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        if flush:
+            flush_l2()
+        att_ev[i][0].record(stream)
+        st.attend()
+        att_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    att_ms = [a.elapsed_time(b) for a, b in att_ev]
+    ms_total = env.max_over_ranks(ms_total)
+    l2 = (f"inputs larger than L2, no flush (KV {kv_unique / 1e9:.2f} GB per step vs 129 MB L2)" if not flush else
+          f"L2 flushed before every step (write {2 * L2_BYTES >> 20} MiB, then read {2 * L2_BYTES >> 20} MiB: "
+          "the step starts with a clean L2); flush time excluded")
+    return {"ms_per_step": ms_total / steps, "attention_ms": statistics.mean(att_ms), "launches": launches,
+            "clocks": clk.summary(), "flush": flush, "l2": l2}
+
+
+def workload_entry(env, name: str, steps: int, warmup: int, seqs: int = 0):
+    """One config under the same clock as the headline: its step and attention
+    times, throughput and roofline fractions.  Frees its device memory after."""
+    torch, pa, W = env.torch, env.pa, env.W
+    wl = make_workload(name, seqs)
+    st = env.pa_setup.upload(wl, device=env.dev)
+    t = time_steps(env, st, wl, steps, warmup)
+    kv_unique = wl.kv_bytes_unique()
+    alg = kv_unique + wl.qo_bytes()
+    alg_step = alg + wl.append_bytes()
+    peak, peak_kind = measured_peaks()
+    att_gbs = alg / (t["attention_ms"] / 1e3) / 1e9
+    step_gbs = alg_step / (t["ms_per_step"] / 1e3) / 1e9
+    src_hash = kernel_source_hash()
+    entry = {
+        "workload": wl.description, "rows": wl.n_rows, "kv_dtype": W.DTYPE_NAMES[wl.kv_dtype],
+        "q_dtype": W.DTYPE_NAMES[wl.q_dtype], "steps": steps, "warmup": warmup,
+        "ms_per_step": t["ms_per_step"], "rows_per_s": wl.n_rows / (t["ms_per_step"] / 1e3),
+        "attention_ms": t["attention_ms"], "kernel": f"{attention_kernel_name(wl)} (pa_attention)",
+        "kv_bytes_unique": kv_unique, "alg_bytes_per_attention": alg, "alg_bytes_per_step": alg_step,
+        "kv_read_gbs": kv_unique / (t["attention_ms"] / 1e3) / 1e9,
+        "achieved_gbs": att_gbs, "frac": att_gbs / peak, "step_gbs": step_gbs, "step_frac": step_gbs / peak,
+        "peak_gbs": peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+        "traffic": profiled_traffic(name, src_hash), "l2": t["l2"], "gpu_launches": t["launches"],
+        "clocks": t["clocks"],
+    }
+    if attention_kernel_name(wl) == "mixed_kernel":
+        entry["prefill_tiles"] = prefill_tiles_alone(pa, torch, st, wl, max(10, min(steps, 50)), env.stream)
+    del st
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_ours(args):
-    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -320,81 +442,22 @@ def run_ours(args):
     else:
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
+    env = Env(torch, pa, W, pa_setup, dist, dev, world, rank)
+    stream = env.stream
 
     wl = make_workload(args.workload, args.seqs)
     st = pa_setup.upload(wl, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step():  # pa_step: the append, then the attention as its programmatic dependent
-        st.step()
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    st.status.zero_()
-
-    # A step whose inputs fit a few times in L2 is timed alone after an L2
-    # flush: write a buffer twice the L2 (evicts everything), then read
-    # another one (so the evicted dirty lines are written back before the
-    # step, not during it).  Larger steps run back to back.
-    kv_unique = wl.kv_bytes_unique()
-    flush = kv_unique <= 4 * L2_BYTES
-    if flush:
-        fl_w = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-        fl_r = torch.ones(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
-
-    def flush_l2():
-        fl_w.fill_(1)
-        fl_r.max()
-
-    # ---- timed region: K steps (one pa_step call each), each bracketed by events
-    ev_start, ev_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    launches0 = pa.kernel_launches()
-    with ClockSampler(dev.index) as clk:
-        barrier()
-        torch.cuda.synchronize()
-        ev_start.record(stream)
-        for i in range(args.steps):
-            if flush:
-                flush_l2()
-            step_ev[i][0].record(stream)
-            step()
-            step_ev[i][1].record(stream)
-        ev_end.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-    launches = pa.kernel_launches() - launches0
-    status = int(st.status.item())
-    if status != 0:
-        raise RuntimeError(f"device status {status} ({pa.status_string(status)}) during the timed steps")
-    # the steps' own device time (the flushes between them excluded)
-    ms_total = sum(a.elapsed_time(b) for a, b in step_ev) if flush else ev_start.elapsed_time(ev_end)
-
-    # ---- the attention launch alone, K times, for its roofline (same flush rule)
-    att_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
-        if flush:
-            flush_l2()
-        att_ev[i][0].record(stream)
-        st.attend()
-        att_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    att_ms = [a.elapsed_time(b) for a, b in att_ev]
-    ms_total = max_over_ranks(ms_total, dist if world > 1 else None, dev)
-    ms_per_step = ms_total / args.steps
+    t = time_steps(env, st, wl, args.steps, args.warmup)
+    ms_per_step = t["ms_per_step"]
     value = job_rows_per_s(wl.n_rows, world, ms_per_step)
+    kv_unique = wl.kv_bytes_unique()
 
     # ---- e2e: the same step through the public API with host buffers
-    pin = lambda t: t.detach().cpu().pin_memory()
+    pin = lambda x: x.detach().cpu().pin_memory()
     h_q, h_k, h_v = pin(st.q), pin(st.k_new), pin(st.v_new)
     h_seq, h_pos, h_bt = pin(st.seq_ids), pin(st.positions), pin(st.block_tables)
     h_out = torch.empty_like(h_q).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_seq, h_pos, h_bt))
+    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_seq, h_pos, h_bt))
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
@@ -404,26 +467,25 @@ def run_ours(args):
         st.seq_ids.copy_(h_seq, non_blocking=True)
         st.positions.copy_(h_pos, non_blocking=True)
         st.block_tables.copy_(h_bt, non_blocking=True)
-        step()
+        st.step()
         h_out.copy_(st.out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
-    barrier()
+    env.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    e2e_ms = max_over_ranks(e2e_ms, dist if world > 1 else None, dev)
+    e2e_ms = env.max_over_ranks(e0.elapsed_time(e1) / args.steps)
     e2e_value = job_rows_per_s(wl.n_rows, world, e2e_ms)
 
     # ---- roofline of the attention kernel
     alg_bytes = kv_unique + wl.qo_bytes()
-    att_avg_ms = statistics.mean(att_ms)
+    att_avg_ms = t["attention_ms"]
     achieved = alg_bytes / (att_avg_ms / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
     src_hash = kernel_source_hash()
@@ -438,6 +500,16 @@ def run_ours(args):
         leg = OracleLeg(wl, target_s=3.0)
         r, _ = leg.step()
         cpu = {"value": r, "unit": "rows/s", "cores": leg.cores, "kind": "oracle", "sample": leg.sample}
+    del st
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    # ---- every other config under the same clock (one process, one GPU)
+    entries = None
+    if world == 1 and not args.no_workloads:
+        entries = {}
+        for name in ALL_WORKLOADS:
+            entries[name] = workload_entry(env, name, max(args.steps, 20), max(args.warmup, 3))
 
     if rank == 0:
         line = {
@@ -446,10 +518,7 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": wl.description, "rows": wl.n_rows, "kv_dtype": W.DTYPE_NAMES[wl.kv_dtype],
                        "q_dtype": W.DTYPE_NAMES[wl.q_dtype], "kv_bytes_unique": kv_unique,
-                       "alg_bytes_per_attention": alg_bytes, "l2": "inputs larger than L2, no flush "
-                       f"(KV {kv_unique / 1e9:.2f} GB per step vs 129 MB L2)" if not flush else
-                       f"L2 flushed before every step (write {2 * L2_BYTES >> 20} MiB, then read "
-                       f"{2 * L2_BYTES >> 20} MiB: the step starts with a clean L2); flush time excluded",
+                       "alg_bytes_per_attention": alg_bytes, "l2": t["l2"],
                        "split_tokens": pa.get_split_tokens(), "parallelism": f"replicas x{world}"},
             "kv_read_gbs": kv_gbs,
             "attention_ms": att_avg_ms,
@@ -460,10 +529,11 @@ def run_ours(args):
                          "kernel_source_hash": src_hash},
             "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
-            "gpu_launches": launches,
+            "gpu_launches": t["launches"],
             **({"prefill_tiles": tiles} if tiles else {}),
-            "clocks": clk.summary(),
+            "clocks": t["clocks"],
             "cpu_baseline": cpu,
+            **({"workloads": entries} if entries is not None else {}),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -480,6 +550,8 @@ def main():
                     choices=sorted(W_CONFIG_NAMES))
     ap.add_argument("--seqs", type=int, default=0, help="shrink the workload to this many sequences (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time the selected workload only (no per-config entries)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

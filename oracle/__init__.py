@@ -183,6 +183,32 @@ def attention(q, q_dtype, num_q_heads, seq_ids, positions, block_tables, num_pag
     return out
 
 
+def workload_pools(wl, rows_of_seqs=None, include_step=True):
+    """The oracle's own pools for a synthetic workload (any object with the
+    fields of workloads.Workload): its append of the history rows (optionally
+    only those that write pages of some sequences), then of the step's rows.
+    Returns (k_pool, v_pool), poisoned where nothing was written."""
+    kp, vp = wl.empty_pool(), wl.empty_pool()
+    hs, hp, hk, hv = wl.hist_seq, wl.hist_pos, wl.hist_k, wl.hist_v
+    if rows_of_seqs is not None:
+        # pages of the chosen sequences may be shared with others (a shared
+        # prefix): keep every history row that writes one of their pages
+        pages = set(int(x) for x in wl.block_tables[list(rows_of_seqs)].reshape(-1) if x >= 0)
+        tgt = wl.block_tables[hs, hp // wl.P]
+        sel = np.isin(tgt, list(pages))
+        hs, hp, hk, hv = hs[sel], hp[sel], hk[sel], hv[sel]
+    st = append(hk, hv, wl.in_dtype, hs, hp, wl.block_tables, wl.num_pages, wl.P, wl.Hkv, wl.D,
+                wl.kv_dtype, wl.k_scale, wl.v_scale, kp, vp)
+    if st != 0:
+        raise ValueError(f"oracle_append (history) failed with status {st}")
+    if include_step:
+        st = append(wl.k_new, wl.v_new, wl.in_dtype, wl.seq_ids, wl.positions, wl.block_tables,
+                    wl.num_pages, wl.P, wl.Hkv, wl.D, wl.kv_dtype, wl.k_scale, wl.v_scale, kp, vp)
+        if st != 0:
+            raise ValueError(f"oracle_append (step) failed with status {st}")
+    return kp, vp
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))

@@ -11,23 +11,7 @@ import workloads as W
 def oracle_pools(wl: W.Workload, rows_of_seqs=None, include_step=True):
     """Oracle append of the history rows (optionally only those of some
     sequences), then of the step's rows.  Returns (k_pool, v_pool)."""
-    kp, vp = wl.empty_pool(), wl.empty_pool()
-    hs, hp, hk, hv = wl.hist_seq, wl.hist_pos, wl.hist_k, wl.hist_v
-    if rows_of_seqs is not None:
-        # pages of the chosen sequences may be shared with others (a shared
-        # prefix): keep every history row that writes one of their pages
-        pages = set(int(x) for x in wl.block_tables[list(rows_of_seqs)].reshape(-1) if x >= 0)
-        tgt = wl.block_tables[hs, hp // wl.P]
-        sel = np.isin(tgt, list(pages))
-        hs, hp, hk, hv = hs[sel], hp[sel], hk[sel], hv[sel]
-    st = oracle.append(hk, hv, wl.in_dtype, hs, hp, wl.block_tables, wl.num_pages, wl.P, wl.Hkv, wl.D,
-                       wl.kv_dtype, wl.k_scale, wl.v_scale, kp, vp)
-    assert st == 0
-    if include_step:
-        st = oracle.append(wl.k_new, wl.v_new, wl.in_dtype, wl.seq_ids, wl.positions, wl.block_tables,
-                           wl.num_pages, wl.P, wl.Hkv, wl.D, wl.kv_dtype, wl.k_scale, wl.v_scale, kp, vp)
-        assert st == 0
-    return kp, vp
+    return oracle.workload_pools(wl, rows_of_seqs=rows_of_seqs, include_step=include_step)
 
 
 def oracle_out(wl: W.Workload, kp, vp, rows=None, n_threads=None):
