@@ -196,13 +196,18 @@ pa_status pa_step(const pa_pool *pool, int32_t n_rows, const void *q, pa_dtype q
  * library's device image: every GPU that loads the library holds it until the
  * process exits, and this call allocates nothing (no cudaMalloc, no cudaFree,
  * no allocating library routine).  Arguments and results are those of
- * pa_attention.  A call whose pa_attention_workspace_bytes(...) exceeds 32 MiB
- * is rejected with PA_ERR_UNSUPPORTED and a message in pa_last_error().
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Every
- * call shares the one array and finds the previous call's contents in it;
- * each call clears the part it uses on `stream` first.  Calls that can run at
- * the same time on the GPU (unordered streams) race on the array. */
+ * pa_attention, checked the same way first.  A call whose split-KV plan (the
+ * bytes pa_attention would need for these rows, chunks, dtypes and split
+ * length) exceeds 32 MiB is rejected with PA_ERR_UNSUPPORTED and a message in
+ * pa_last_error(); the split length is read once per call.
+ * The first call on a device that needs the array looks up its device
+ * address (with that device current), and looks it up again when the
+ * device's CUDA context has changed since (after cudaDeviceReset, for
+ * instance); make that first call before any stream capture.  Every call
+ * shares the one array and finds the previous call's contents in it; each
+ * call clears its plan's split counters on `stream` first (every other byte
+ * it reads, it has written).  Calls that can run at the same time on the GPU
+ * (unordered streams) race on the array. */
 pa_status pa_attention_noalloc(const pa_pool *pool, int32_t n_rows, const void *q, pa_dtype q_dtype,
                                int32_t num_q_heads, const int32_t *seq_ids, const int32_t *positions,
                                const int32_t *block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,

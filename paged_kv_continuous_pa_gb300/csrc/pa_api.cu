@@ -266,12 +266,16 @@ pa_status build_append(const pa_pool* pool, int32_t n_rows, const void* k_new, c
 // once every attention argument has passed its checks, and the attention
 // kernel follows it as a programmatic dependent: its CTAs start their
 // query, sequence and page-id lookups while the append runs, and wait for it
-// before the first pool read.
+// before the first pool read.  With `scratch` (pa_attention_noalloc) the
+// workspace is the library's fixed scratch array instead of the caller's:
+// the plan must fit in it, and the call clears the plan's split counters on
+// the stream before its launch.
 pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_dtype q_dtype, int32_t num_q_heads,
                          const int32_t* seq_ids, const int32_t* positions, const int32_t* block_tables,
                          int32_t num_seqs, int32_t max_blocks_per_seq, const pa_chunk* chunks, int32_t n_chunks,
                          float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
-                         int32_t* status_dev, void* stream, const pa::AppendParams* pre) {
+                         int32_t* status_dev, void* stream, const pa::AppendParams* pre,
+                         const pa::FixedScratch* scratch = nullptr) {
   if (pool == nullptr) return fail(PA_ERR_INVALID_ARG, "pool is NULL");
   const pa_pool_desc& d = pool->desc;
   if (n_rows < 0) return fail(PA_ERR_INVALID_ARG, "n_rows %d < 0", n_rows);
@@ -307,6 +311,16 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
   const int32_t split_tokens = g_split_tokens.load(std::memory_order_relaxed);  // one value for the plan and the kernels
   const Plan pl = make_plan(d, n_rows, num_q_heads, max_blocks_per_seq, chunks, n_chunks,
                             q_dtype == PA_BF16 && d.kv_dtype == PA_BF16, split_tokens);
+  if (scratch != nullptr && pl.total > 0) {
+    if (pl.total > scratch->bytes)
+      return fail(PA_ERR_UNSUPPORTED,
+                  "pa_attention_noalloc: this call needs %zu bytes of split-KV scratch but the static scratch holds "
+                  "%zu; use pa_attention with a caller workspace, fewer rows or a shorter block table",
+                  pl.total, scratch->bytes);
+    workspace = scratch->address();
+    if (workspace == nullptr) return PA_ERR_CUDA;  // the lookup set the message
+    workspace_bytes = scratch->bytes;
+  }
   if (pl.total > 0) {
     if (workspace == nullptr || workspace_bytes < pl.total)
       return fail(PA_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", pl.total,
@@ -398,6 +412,19 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
   }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (scratch != nullptr && pl.total > 0) {
+    // the counters of the finished splits must start at zero; every partial
+    // is written before it is read, so nothing else needs clearing
+    unsigned char* base = static_cast<unsigned char*>(workspace);
+    if (pl.max_splits > 1) {
+      const cudaError_t e = cudaMemsetAsync(base + pl.d_count, 0, static_cast<size_t>(n_rows) * d.num_kv_heads * 4, s);
+      if (e != cudaSuccess) return cuda_fail(e, "pa_attention_noalloc: clearing the split counters");
+    }
+    if (pl.tile_splits > 1) {
+      const cudaError_t e = cudaMemsetAsync(base + pl.t_count, 0, static_cast<size_t>(pl.total_tiles) * 4, s);
+      if (e != cudaSuccess) return cuda_fail(e, "pa_attention_noalloc: clearing the tile counters");
+    }
+  }
   if (pre != nullptr) {
     const cudaError_t ea = pa::launch_append(*pre, s);
     if (ea != cudaSuccess) return cuda_fail(ea, "append launch");
@@ -423,6 +450,16 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
 }
 
 }  // namespace
+
+pa_status pa::attention_fixed_scratch(const pa_pool* pool, int32_t n_rows, const void* q, pa_dtype q_dtype,
+                                      int32_t num_q_heads, const int32_t* seq_ids, const int32_t* positions,
+                                      const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                                      const pa_chunk* chunks, int32_t n_chunks, float softmax_scale, void* out,
+                                      int32_t* status_dev, void* stream, const FixedScratch& scratch) {
+  return attention_impl(pool, n_rows, q, q_dtype, num_q_heads, seq_ids, positions, block_tables, num_seqs,
+                        max_blocks_per_seq, chunks, n_chunks, softmax_scale, out, nullptr, 0, status_dev, stream,
+                        nullptr, &scratch);
+}
 
 extern "C" {
 

@@ -8,6 +8,8 @@
 
 #include <atomic>
 
+#include "../../include/pa.h"
+
 namespace pa {
 
 constexpr int kMaxChunks = 16;          // prefill chunks per pa_attention call
@@ -174,6 +176,24 @@ inline cudaError_t launch_kernel(Kernel kernel, dim3 grid, dim3 block, size_t sm
 
 // Process-wide count of kernel launches made by the library (pa_kernel_launches).
 void count_launch();
+
+// A scratch array of `bytes` bytes that the library owns (pa_attention_noalloc):
+// address() returns its device address on the current device, or nullptr
+// after setting the last-error text.
+struct FixedScratch {
+  size_t bytes;
+  void* (*address)();
+};
+
+// pa_attention with `scratch` as its workspace: the arguments are checked as
+// pa_attention checks them, the plan is made once (one read of the split
+// length), a plan larger than the scratch is refused with PA_ERR_UNSUPPORTED,
+// and the plan's split counters are cleared on `stream` before the launch.
+pa_status attention_fixed_scratch(const pa_pool* pool, int32_t n_rows, const void* q, pa_dtype q_dtype,
+                                  int32_t num_q_heads, const int32_t* seq_ids, const int32_t* positions,
+                                  const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                                  const pa_chunk* chunks, int32_t n_chunks, float softmax_scale, void* out,
+                                  int32_t* status_dev, void* stream, const FixedScratch& scratch);
 
 // Set the calling thread's pa_last_error() text.
 void set_last_error(const char* fmt, ...);

@@ -11,10 +11,13 @@
 // kNoallocScratchBytes of it until the process exits.
 //
 // The array is shared by every call on a device and keeps the last call's
-// contents; each call clears the part it uses on its stream before the
-// attention launch.  Calls that overlap on the GPU (different streams, no
-// ordering between them) race on it.
+// contents; each call clears the split counters of its plan on its stream
+// before the attention launch (every partial is written before it is read).
+// Calls that overlap on the GPU (different streams, no ordering between them)
+// race on it.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -31,12 +34,35 @@ constexpr int kMaxDevices = 64;
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_dev[kMaxDevices] = {};
+// The address found for a device, and the context it was found in: a device
+// reset (or a primary context released and created again) gives the device a
+// new context, where the array has a new address, so the lookup is repeated.
+struct CachedAddress {
+  CUcontext ctx;
+  void* ptr;
+};
 
-// Device address of the scratch array on the current device, looked up once
-// per device (the first call on a device does it, with that device current).
-// Returns nullptr (and sets the last-error text) on failure.
+std::mutex g_mu;
+CachedAddress g_scratch_dev[kMaxDevices] = {};
+
+// cuCtxGetCurrent from the driver, looked up once through the runtime.
+PFN_cuCtxGetCurrent_v4000 ctx_getter() {
+  static std::once_flag once;
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(ptr);
+  });
+  return fn;
+}
+
+// Device address of the scratch array on the current device, looked up with
+// that device current the first time a call needs it there (and again after
+// the device's context changed).  Returns nullptr (and sets the last-error
+// text) on failure.
 void* scratch_on_current_device() {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -44,18 +70,31 @@ void* scratch_on_current_device() {
     pa::set_last_error("pa_attention_noalloc: no current CUDA device (%s)", cudaGetErrorString(e));
     return nullptr;
   }
+  PFN_cuCtxGetCurrent_v4000 get = ctx_getter();
+  if (get == nullptr) {
+    pa::set_last_error("pa_attention_noalloc: cuCtxGetCurrent is not available from the driver");
+    return nullptr;
+  }
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_dev[dev] == nullptr) {
+  CachedAddress& c = g_scratch_dev[dev];
+  if (ctx == nullptr || c.ptr == nullptr || c.ctx != ctx) {
     void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);  // makes the device's context current if none was
     if (e != cudaSuccess || ptr == nullptr) {
       pa::set_last_error("pa_attention_noalloc: cudaGetSymbolAddress failed on device %d (%s)", dev,
                          cudaGetErrorString(e));
       return nullptr;
     }
-    g_scratch_dev[dev] = ptr;
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+      pa::set_last_error("pa_attention_noalloc: cannot read the current CUDA context on device %d", dev);
+      return nullptr;
+    }
+    c.ctx = ctx;
+    c.ptr = ptr;
   }
-  return g_scratch_dev[dev];
+  return c.ptr;
 }
 
 }  // namespace
@@ -65,24 +104,8 @@ extern "C" pa_status pa_attention_noalloc(const pa_pool* pool, int32_t n_rows, c
                                           const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
                                           const pa_chunk* chunks, int32_t n_chunks, float softmax_scale, void* out,
                                           int32_t* status_dev, void* stream) {
-  const size_t need = pa_attention_workspace_bytes(pool, n_rows, num_q_heads, max_blocks_per_seq, chunks, n_chunks);
-  if (need > kNoallocScratchBytes) {
-    pa::set_last_error(
-        "pa_attention_noalloc: this call needs %zu bytes of split-KV scratch but the static scratch holds %zu; "
-        "use pa_attention with a caller workspace, fewer rows or a shorter block table",
-        need, kNoallocScratchBytes);
-    return PA_ERR_UNSUPPORTED;
-  }
-  void* scratch = nullptr;
-  if (need > 0) {
-    scratch = scratch_on_current_device();
-    if (scratch == nullptr) return PA_ERR_CUDA;
-    cudaError_t e = cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
-      pa::set_last_error("pa_attention_noalloc: clearing the scratch failed (%s)", cudaGetErrorString(e));
-      return PA_ERR_CUDA;
-    }
-  }
-  return pa_attention(pool, n_rows, q, q_dtype, num_q_heads, seq_ids, positions, block_tables, num_seqs,
-                      max_blocks_per_seq, chunks, n_chunks, softmax_scale, out, scratch, need, status_dev, stream);
+  const pa::FixedScratch scratch{kNoallocScratchBytes, &scratch_on_current_device};
+  return pa::attention_fixed_scratch(pool, n_rows, q, q_dtype, num_q_heads, seq_ids, positions, block_tables,
+                                     num_seqs, max_blocks_per_seq, chunks, n_chunks, softmax_scale, out, status_dev,
+                                     stream, scratch);
 }

@@ -198,3 +198,24 @@ def test_status_strings(lib):
     for code, name in enumerate(["PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED", "PA_ERR_OUT_OF_RANGE",
                                  "PA_ERR_TIMEOUT", "PA_ERR_CUDA", "PA_ERR_NO_PAGES"]):
         assert pa.status_string(code) == name
+
+
+def test_noalloc_checks_arguments_then_its_scratch_size(lib):
+    """pa_attention_noalloc checks its arguments as pa_attention does before it
+    sizes its plan: a chunk of no rows is an invalid argument (not an
+    unsupported size), and a plan beyond the 32 MiB scratch is refused before
+    any CUDA call."""
+    st, h = _create(lib, _desc(head_dim=128, num_kv_heads=8))
+    assert st == pa.PA_OK
+    try:
+        dev = ctypes.c_void_p(0x100000)
+        bad = (pa.Chunk * 1)(pa.Chunk(0, 0))
+        assert lib.pa_attention_noalloc(h, 4, dev, pa.PA_BF16, 16, dev, dev, dev, 4, 2048, bad, 1, 0.0, dev, None,
+                                        None) == pa.PA_ERR_INVALID_ARG
+        assert "chunk" in pa.last_error()
+        # 4096 rows x 64 splits of 16 heads: far more than 32 MiB of partials
+        assert lib.pa_attention_noalloc(h, 4096, dev, pa.PA_BF16, 16, dev, dev, dev, 4096, 2048, None, 0, 0.0, dev,
+                                        None, None) == pa.PA_ERR_UNSUPPORTED
+        assert "scratch" in pa.last_error()
+    finally:
+        lib.pa_pool_destroy(h)

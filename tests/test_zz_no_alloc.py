@@ -2,9 +2,15 @@
 memory (they are handed only input and output buffers, for instance by a
 host runtime that owns all device memory, or may not call cudaMalloc on the
 serving path).  Its split-KV scratch is a fixed 32 MiB array inside the
-library.  Checked through the C ABI against pa_attention, which takes a
-caller workspace, on two calls in a row (the second with a different batch,
-so leftovers of the first call in the shared array would show)."""
+library.
+
+Both entry points run the same kernels on the same plan, so their outputs must
+be byte-identical: a tolerance would hide partials or counters left over in the
+shared array by an earlier call.  Checked through the C ABI against
+pa_attention (which takes a caller workspace) on two calls in a row, the
+second with a different batch, and against the oracle; and through the Python
+binding on a step whose chunk's key range is split across CTAs, so that the
+tile path's partials and counters go through the shared array too."""
 import ctypes
 
 import numpy as np
@@ -15,7 +21,7 @@ import pa_setup
 import paged_kv_continuous_pa_gb300 as pa
 import workloads as W
 from paged_kv_continuous_pa_gb300 import build as pa_build
-from ref import assert_close
+from ref import assert_close, oracle_out, oracle_pools
 
 pytestmark = pytest.mark.gpu
 
@@ -29,15 +35,22 @@ def _noalloc_raw(lib, st, q, seq, pos, out):
                                     torch.cuda.current_stream().cuda_stream)
 
 
+def _bits(t):
+    return t.view(torch.int16).cpu().numpy().tobytes()
+
+
+def _with_split(tokens, fn):
+    old = pa.get_split_tokens()
+    pa.set_split_tokens(tokens)
+    try:
+        fn()
+    finally:
+        pa.set_split_tokens(old)
+
+
 def test_noalloc_matches_workspace_entry_point_twice():
     pa_build.build()
-    lib = pa.load()
-    old_split = pa.get_split_tokens()
-    pa.set_split_tokens(1024)  # so that the rows are split and the scratch is used
-    try:
-        _compare_twice(lib)
-    finally:
-        pa.set_split_tokens(old_split)
+    _with_split(1024, lambda: _compare_twice(pa.load()))  # rows longer than 1024 keys are split
 
 
 def _compare_twice(lib):
@@ -46,6 +59,7 @@ def _compare_twice(lib):
     st.append_step()
     torch.cuda.synchronize()
     assert pa.workspace_bytes(st.pool, wl.n_rows, wl.Hq, wl.max_blocks) > 0
+    kp, vp = oracle_pools(wl)
 
     batches = [np.arange(wl.n_rows), np.random.default_rng(1).permutation(wl.n_rows)[:29]]
     for call, rows in enumerate(batches):
@@ -62,9 +76,42 @@ def _compare_twice(lib):
         assert _noalloc_raw(lib, st, q, seq, pos, out) == pa.PA_OK, pa.last_error()
         torch.cuda.synchronize()
         assert int(st.status.item()) == 0
-        got = W.bf16_bits_to_f32(pa_setup.to_numpy(out)).astype(np.float64)
-        ref = W.bf16_bits_to_f32(pa_setup.to_numpy(ref_out)).astype(np.float64)
-        assert_close(got, ref, wl, f"noalloc call {call + 1}")
+        assert _bits(out) == _bits(ref_out), f"noalloc call {call + 1}: output bytes differ from pa_attention"
+        if call == 0:
+            got = W.bf16_bits_to_f32(pa_setup.to_numpy(out)).astype(np.float64)
+            assert_close(got, oracle_out(wl, kp, vp, rows=rows), wl, "noalloc against the oracle")
+
+
+def test_noalloc_tile_splits_through_the_binding_twice():
+    """A bf16 step whose 64-row chunk reads 4264 keys (its key range is split
+    across two CTAs per tile, more than 4096 keys) beside decode rows split at
+    1024 keys: both kinds of partials and counters use the shared array."""
+    pa_build.build()
+    _with_split(1024, _tile_case)
+
+
+def _tile_case():
+    wl = W.chunked_step(61, chunks=[(4200, 64, 4300)], decode_ctx=[3000, 5000, 17])
+    assert wl.max_blocks * wl.P > 4096
+    st = pa_setup.upload(wl)
+    st.append_step()
+    torch.cuda.synchronize()
+    kp, vp = oracle_pools(wl)
+    ref_out = torch.empty_like(st.q)
+    ws_bytes = pa.workspace_bytes(st.pool, wl.n_rows, wl.Hq, wl.max_blocks, wl.chunks)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    pa.attention(st.pool, st.q, st.seq_ids, st.positions, st.block_tables, ref_out, chunks=wl.chunks, workspace=ws,
+                 status=st.status)
+    for call in range(2):
+        out = torch.full_like(st.q, float("nan"))
+        st.status.zero_()
+        pa.attention_noalloc(st.pool, st.q, st.seq_ids, st.positions, st.block_tables, out, chunks=wl.chunks,
+                             status=st.status)
+        torch.cuda.synchronize()
+        assert int(st.status.item()) == 0
+        assert _bits(out) == _bits(ref_out), f"noalloc call {call + 1}: output bytes differ from pa_attention"
+    got = W.bf16_bits_to_f32(pa_setup.to_numpy(out)).astype(np.float64)
+    assert_close(got, oracle_out(wl, kp, vp), wl, "noalloc tile splits against the oracle")
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch():
@@ -78,4 +125,5 @@ def test_noalloc_rejects_calls_beyond_its_scratch():
     st = lib.pa_attention_noalloc(pool.handle, n, dev, pa.PA_BF16, hq, dev, dev, dev, n, mb, None, 0, 0.0, dev,
                                   None, None)
     assert st == pa.PA_ERR_UNSUPPORTED
-    assert "32" in pa.last_error() or "scratch" in pa.last_error()
+    assert "scratch" in pa.last_error()
+
