@@ -166,20 +166,28 @@ pa_status pa_attention(const pa_pool *pool, int32_t n_rows, const void *q, pa_dt
                        void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream);
 
 /* One decode/prefill step: pa_append_kv of the step's rows, then pa_attention
- * over the same rows, as two launches on `stream` in which the attention kernel
- * is a programmatic dependent of the append: its CTAs start (query, sequence
- * and page-id lookups) while the append runs and wait for the append's
- * completion before their first read of the pools.  Between the two launches
- * of a step the pages put the launch gap of eager decoding ("Building an LLM
- * runtime from scratch on NVIDIA H100", section "Bug #2: Eager Decode and the
- * CUDA Graph Necessity"; "GPU inference engine engineering", section "Speed
- * that counts end to end"); this removes the attention's start-up latency from
- * the step, and the pair stays capturable in a CUDA graph.
+ * over the same rows ("GPU inference engine engineering", section "Speed that
+ * counts end to end": fewer launches per step; "Building an LLM runtime from
+ * scratch on NVIDIA H100", section "Bug #2: Eager Decode and the CUDA Graph
+ * Necessity": the launch gaps of eager decoding).
+ *   - Rows outside every chunk (decode rows) append their own new K/V inside
+ *     the attention launch: for each kv head, the attention unit that holds
+ *     the row's position stores the row's converted key and value in the pool
+ *     before it copies that page, so a step without chunks is ONE launch.
+ *   - Chunk rows read one another's keys, so they are appended first by an
+ *     append launch over the chunks' rows only; the attention kernel is its
+ *     programmatic dependent (its CTAs start their lookups while the append
+ *     runs; chunk tiles and chunk rows wait for it before reading the pools,
+ *     decode rows do not wait).
+ * Precondition (beyond those of pa_append_kv and pa_attention): a row outside
+ * every chunk is the only row of its sequence in the step; a sequence that
+ * contributes several rows to one step lists them as a chunk.
  *   k_new, v_new, kv_in_dtype: as pa_append_kv's k_new, v_new, in_dtype
  *   the other arguments: as pa_attention
- * Results are bit-identical to pa_append_kv followed by pa_attention on the
- * same stream.  Every argument of both is checked before anything is
- * launched; errors as for those two calls. */
+ * Results (pool bytes and outputs) are bit-identical to pa_append_kv followed
+ * by pa_attention on the same stream.  Every argument of both is checked
+ * before anything is launched; errors as for those two calls.  Capturable in
+ * a CUDA graph. */
 pa_status pa_step(const pa_pool *pool, int32_t n_rows, const void *q, pa_dtype q_dtype, int32_t num_q_heads,
                   const void *k_new, const void *v_new, pa_dtype kv_in_dtype, const int32_t *seq_ids,
                   const int32_t *positions, const int32_t *block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,

@@ -426,9 +426,32 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
     }
   }
   if (pre != nullptr) {
-    const cudaError_t ea = pa::launch_append(*pre, s);
-    if (ea != cudaSuccess) return cuda_fail(ea, "append launch");
-    p.dependent = 1;
+    // pa_step: rows outside the chunks append their own K/V inside the
+    // attention launch (each is its sequence's only row in the step); the
+    // chunks' rows, which read one another's keys, are appended first by a
+    // launch the attention depends on.  No chunks: one launch.
+    p.fuse_append = 1;
+    p.in_dtype = pre->in_dtype;
+    p.k_new = pre->k_new;
+    p.v_new = pre->v_new;
+    for (int h = 0; h < pa::kMaxHeadScales; ++h) p.k_enc_scale_h[h] = pre->k_scale_h[h];
+    p.n_all_chunks = n_chunks;
+    for (int c = 0; c < n_chunks; ++c) {
+      p.all_chunk_begin[c] = chunks[c].row_begin;
+      p.all_chunk_end[c] = chunks[c].row_begin + chunks[c].n_rows;
+    }
+    if (n_chunks > 0) {
+      pa::AppendParams ap = *pre;
+      ap.n_ranges = n_chunks;
+      ap.range_first[0] = 0;
+      for (int c = 0; c < n_chunks; ++c) {
+        ap.range_begin[c] = chunks[c].row_begin;
+        ap.range_first[c + 1] = ap.range_first[c] + chunks[c].n_rows;
+      }
+      const cudaError_t ea = pa::launch_append(ap, s);
+      if (ea != cudaSuccess) return cuda_fail(ea, "append launch");
+      p.dependent = 1;
+    }
   }
   cudaError_t e = cudaErrorNotSupported;
   if (p.n_prefill_ctas > 0) {

@@ -19,9 +19,15 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
   griddep_launch_dependents();  // an attention launched as a dependent may start its lookups now
   const long long oct_per_row = static_cast<long long>(p.Hkv) * p.D / 8;  // octets of one K (or V) row
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long total = static_cast<long long>(p.n_rows) * 2 * oct_per_row;
+  const long long rows = p.n_ranges > 0 ? p.range_first[p.n_ranges] : p.n_rows;
+  const long long total = rows * 2 * oct_per_row;
   if (idx >= total) return;
-  const long long row = idx / (2 * oct_per_row);
+  long long row = idx / (2 * oct_per_row);
+  if (p.n_ranges > 0) {  // the i-th row of the ranges
+    int k = 0;
+    while (k + 1 < p.n_ranges && row >= p.range_first[k + 1]) ++k;
+    row = p.range_begin[k] + (row - p.range_first[k]);
+  }
   const long long rem = idx % (2 * oct_per_row);
   const bool is_v = rem >= oct_per_row;
   const long long oct = is_v ? rem - oct_per_row : rem;  // octet within [Hkv][D]
@@ -77,27 +83,20 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
   } else if (p.kv_dtype == KV_BF16) {
     uint32_t o[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(x[2 * i]));
-      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(x[2 * i + 1]));
-      o[i] = lo | (hi << 16);
-    }
+    for (int i = 0; i < 4; ++i) o[i] = encode_bf16(x[2 * i]) | (encode_bf16(x[2 * i + 1]) << 16);
     *reinterpret_cast<uint4*>(static_cast<uint16_t*>(pool) + dst) = make_uint4(o[0], o[1], o[2], o[3]);
   } else {
     const float scale = is_v ? p.v_scale_h[PA_HEAD(p, h)] : p.k_scale_h[PA_HEAD(p, h)];
     uint32_t o[2] = {0u, 0u};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float qv = __fdiv_rn(x[i], scale);
-      const uint32_t code = __nv_cvt_float_to_fp8(qv, __NV_SATFINITE, __NV_E4M3);
-      o[i / 4] |= (code & 0xffu) << (8 * (i % 4));
-    }
+    for (int i = 0; i < 8; ++i) o[i / 4] |= encode_e4m3(x[i], scale) << (8 * (i % 4));
     *reinterpret_cast<uint2*>(static_cast<uint8_t*>(pool) + dst) = make_uint2(o[0], o[1]);
   }
 }
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
-  const long long total = static_cast<long long>(p.n_rows) * 2 * p.Hkv * p.D / 8;
+  const long long rows = p.n_ranges > 0 ? p.range_first[p.n_ranges] : p.n_rows;
+  const long long total = rows * 2 * p.Hkv * p.D / 8;
   if (total <= 0) return cudaSuccess;
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;

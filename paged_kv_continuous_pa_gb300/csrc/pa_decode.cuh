@@ -56,6 +56,109 @@ struct KvElt<KV_E4M3> {
   static constexpr int bytes = 1;
 };
 
+// ------------------------------------------------ a row's own K/V append --
+//
+// In a pa_step, a row outside every chunk the caller listed is the only row
+// of its sequence in the step, so no other row reads the slot its append
+// writes.  Its attention units therefore append it themselves: the unit of
+// its last split (per kv head) loads the row's new key and value when it
+// starts, converts them exactly as the append kernel would, stores them in
+// the pool, and writes the same bytes over that slot in its own shared-memory
+// stage once the stage has landed (the copy may have read the slot before the
+// store).  Nothing waits for the append, and such rows wait for no preceding
+// launch.
+
+__device__ __forceinline__ bool row_appends_itself(const AttnParams& p, int row) {
+  if (!p.fuse_append) return false;
+  for (int c = 0; c < p.n_all_chunks; ++c)
+    if (row >= p.all_chunk_begin[c] && row < p.all_chunk_end[c]) return false;
+  return true;
+}
+
+// Elements d0 .. d0 + E - 1 of row `row`, kv head h of the step's new K
+// (is_v false) or V, as loaded: E f32 words, or E / 2 words of bf16 pairs.
+template <int E>
+__device__ __forceinline__ void load_new_raw(const AttnParams& p, int row, int h, int d0, bool is_v,
+                                             uint32_t (&raw)[4]) {
+  static_assert(E == 2 || E == 4, "elements per lane");
+  const size_t i = (static_cast<size_t>(row) * p.Hkv + h) * p.D + d0;
+  const void* src = is_v ? p.v_new : p.k_new;
+  raw[0] = raw[1] = raw[2] = raw[3] = 0u;
+  if (p.in_dtype == KV_F32) {
+    const float* f = static_cast<const float*>(src) + i;
+    if constexpr (E == 4) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(f));
+      raw[0] = a.x; raw[1] = a.y; raw[2] = a.z; raw[3] = a.w;
+    } else {
+      const uint2 a = __ldg(reinterpret_cast<const uint2*>(f));
+      raw[0] = a.x; raw[1] = a.y;
+    }
+  } else {
+    const uint16_t* b = static_cast<const uint16_t*>(src) + i;
+    if constexpr (E == 4) {
+      const uint2 a = __ldg(reinterpret_cast<const uint2*>(b));
+      raw[0] = a.x; raw[1] = a.y;
+    } else {
+      raw[0] = __ldg(reinterpret_cast<const uint32_t*>(b));
+    }
+  }
+}
+
+// Those elements in the pool's storage format: the input bits when the
+// dtypes match, else the append kernel's conversion.  Packed little-endian
+// into w (E * element bytes: 2 .. 16).
+template <int KVT, int E>
+__device__ __forceinline__ void convert_new(const AttnParams& p, int h, bool is_v, const uint32_t (&raw)[4],
+                                            uint32_t (&w)[4]) {
+  w[0] = w[1] = w[2] = w[3] = 0u;
+  const bool in_f32 = p.in_dtype == KV_F32;
+  if constexpr (KVT == KV_F32) {
+    if (in_f32) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) w[e] = raw[e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) w[e] = __float_as_uint((e & 1) ? bf16hi(raw[e / 2]) : bf16lo(raw[e / 2]));
+    }
+  } else if constexpr (KVT == KV_BF16) {
+    if (in_f32) {
+#pragma unroll
+      for (int e = 0; e < E; e += 2)
+        w[e / 2] = encode_bf16(__uint_as_float(raw[e])) | (encode_bf16(__uint_as_float(raw[e + 1])) << 16);
+    } else {
+#pragma unroll
+      for (int e = 0; e < E / 2; ++e) w[e] = raw[e];
+    }
+  } else {
+    const float scale = is_v ? p.v_scale_h[PA_HEAD(p, h)] : p.k_enc_scale_h[PA_HEAD(p, h)];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float x = in_f32 ? __uint_as_float(raw[e]) : ((e & 1) ? bf16hi(raw[e / 2]) : bf16lo(raw[e / 2]));
+      w[0] |= encode_e4m3(x, scale) << (8 * e);
+    }
+  }
+}
+
+// Store BYTES (2 .. 16) bytes of w at dst (aligned to BYTES).
+template <int BYTES>
+__device__ __forceinline__ void store_piece(void* dst, const uint32_t (&w)[4]) {
+  if constexpr (BYTES == 16)
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  else if constexpr (BYTES == 8)
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  else if constexpr (BYTES == 4)
+    *reinterpret_cast<uint32_t*>(dst) = w[0];
+  else
+    *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w[0]);
+}
+
+// Byte address, in a pool, of element d of slot `slot` of page `page`, kv head h.
+__device__ __forceinline__ unsigned char* pool_elem(const void* pool, const AttnParams& p, int page, int h, int slot,
+                                                    int d, int elt) {
+  const size_t e = ((static_cast<size_t>(page) * p.Hkv + h) * p.P + slot) * p.D + d;
+  return const_cast<unsigned char*>(static_cast<const unsigned char*>(pool)) + e * elt;
+}
+
 // Compile-time geometry of one decode instantiation.
 //   QK layout: LPT lanes share one token; each holds D / LPT elements of the G
 //   query vectors in registers.  A warp scores TPS tokens per sub-step and U
@@ -109,6 +212,7 @@ struct DecodeSmemHeader {
   int32_t issued;              // stages issued so far
   int32_t pid[kMaxUnitPages];  // the unit's physical page ids
   alignas(16) float p[kDecodeWarps][kStageTokens / kDecodeWarps][8];  // softmax weights: [warp][token][head]
+  alignas(16) uint32_t own[2][128];  // the row's own new K and V row in pool format (a row that appends itself)
 };
 
 __host__ __device__ constexpr size_t decode_header_bytes() { return (sizeof(DecodeSmemHeader) + 127) / 128 * 128; }
@@ -525,6 +629,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
   if (p.n_chunks > 0 && row_in_chunk(p, row)) return;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool own_row = row_appends_itself(p, row);
   const int seq = __ldg(p.seq_ids + row);
   const int pos = __ldg(p.positions + row);
   const bool q_bf16 = p.q_is_bf16 != 0;
@@ -550,6 +655,22 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
   const int nstage = (t_end - t_begin + ST - 1) / ST;
   constexpr int NST = Geo::STAGES;
   const int lg_p = 31 - __clz(P);
+
+  // this row's own K/V append (pa_step): in the unit of the last split, the
+  // warp that owns the row's slot in the last stage loads the row's new K and V
+  // (E elements a lane), converts them, stores them in the pool, and copies
+  // them into that stage once it has landed
+  constexpr int E = D / 32;
+  constexpr int PB = E * Geo::ELT;  // bytes of a lane's piece
+  const bool appends = own_row && split == nsplit - 1;
+  // the stage in which this warp writes the row's slot: the last, for the warp
+  // that owns the slot there (-1: none)
+  const int patch_n = (appends && warp == (pos - (t_begin + (nstage - 1) * ST)) / WT) ? nstage - 1 : -1;
+  uint32_t kraw[4], vraw[4];  // that warp's lanes: E elements each of the row's new K and V, loaded now
+  if (patch_n >= 0) {
+    load_new_raw<E>(p, row, h, E * lane, false, kraw);
+    load_new_raw<E>(p, row, h, E * lane, true, vraw);
+  }
 
   DecodeSmemHeader* hdr = reinterpret_cast<DecodeSmemHeader*>(smem);
   unsigned char* ring = smem + decode_header_bytes();
@@ -582,11 +703,28 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
   sync_threads_n<Geo::THREADS>();
   const bool unit_bad = hdr->bad != 0;
   const uint64_t policy = l2_policy_evict_first();
-  griddep_wait();  // the pool rows appended by a preceding dependent-launch append are visible from here
+  // the pool rows appended by a preceding dependent-launch append are visible
+  // from here (a row that appends itself reads nothing that launch writes)
+  if (!own_row) griddep_wait();
   if (tid == 0 && !unit_bad) {
     const int first = min(NST, nstage);
     for (int n = 0; n < first; ++n) issue_stage<RB>(p, hdr, ring, n, n, t_begin, t_end, j0, h, lg_p, policy);
     hdr->issued = first;
+  }
+  if (patch_n >= 0) {
+    // the row's own K/V, converted, to the pool, and to the header for this
+    // warp's copy into the stage once it has landed
+    uint32_t kw[4], vw[4];
+    convert_new<KVT, E>(p, h, false, kraw, kw);
+    convert_new<KVT, E>(p, h, true, vraw, vw);
+    const int pid = hdr->pid[(pos >> lg_p) - j0];
+    if (pid >= 0 && pid < p.num_pages) {
+      store_piece<PB>(pool_elem(p.k_pool, p, pid, h, pos & (P - 1), E * lane, Geo::ELT), kw);
+      store_piece<PB>(pool_elem(p.v_pool, p, pid, h, pos & (P - 1), E * lane, Geo::ELT), vw);
+    }
+    store_piece<PB>(reinterpret_cast<unsigned char*>(hdr->own[0]) + PB * lane, kw);
+    store_piece<PB>(reinterpret_cast<unsigned char*>(hdr->own[1]) + PB * lane, vw);
+    __syncwarp();
   }
 
   // ---- per-warp state
@@ -634,6 +772,17 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
     }
     const unsigned char* ks = ring + static_cast<size_t>(s) * 2 * ST * RB + static_cast<size_t>(wtok0) * RB;
     const unsigned char* vs = ks + ST * RB;
+    if (n == patch_n) {  // the row's own slot, as appended (this warp alone reads it)
+      const size_t off = static_cast<size_t>(pos - (t_begin + n * ST) - wtok0) * RB + PB * lane;
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      for (int i = 0; i < PB / 4; ++i) w[i] = hdr->own[0][(PB / 4) * lane + i];
+      if constexpr (PB < 4) w[0] = reinterpret_cast<const uint16_t*>(hdr->own[0])[lane];
+      store_piece<PB>(const_cast<unsigned char*>(ks) + off, w);
+      for (int i = 0; i < PB / 4; ++i) w[i] = hdr->own[1][(PB / 4) * lane + i];
+      if constexpr (PB < 4) w[0] = reinterpret_cast<const uint16_t*>(hdr->own[1])[lane];
+      store_piece<PB>(const_cast<unsigned char*>(vs) + off, w);
+      __syncwarp();
+    }
     const int n_valid = min(WT, t_end - (t_begin + n * ST + wtok0));
     if (n_valid == WT)
       decode_stage<D, G, KVT, true>(st, ks, vs, pbuf, WT, tok, part, pv_tok, pv_off);

@@ -175,6 +175,15 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
       qraw[kb][1] = __ldg(qs + 8 * kb + 4 + t4);
     }
   }
+  // a row that appends itself (pa_step): lane l loads elements 4l .. 4l+3 of
+  // its new K and V before anything else, so that they have landed by the
+  // time the page ids have
+  const bool own_row = row_appends_itself(p, row);
+  uint32_t kw[4], vw[4];
+  if (own_row) {
+    load_new_raw<4>(p, row, h, 4 * lane, false, kw);
+    load_new_raw<4>(p, row, h, 4 * lane, true, vw);
+  }
   const int seq = __ldg(p.seq_ids + row);
   const int pos = __ldg(p.positions + row);
   const bool q_bf16 = p.q_is_bf16 != 0;  // always true here: the tensor-core units take bf16 queries
@@ -196,6 +205,7 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
   const int npg = (t_end + P - 1) / P - j0;
   const int nstage = (t_end - t_begin + ST - 1) / ST;
   const int lg_p = 31 - __clz(P);
+  const bool append_here = own_row && split == nsplit - 1;
 
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   MmaSmemHeader* hdr = reinterpret_cast<MmaSmemHeader*>(smem);
@@ -224,10 +234,23 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
       record_error(p.status, ST_OUT_OF_RANGE);
     }
   }
-  griddep_wait();  // the pool rows appended by a preceding dependent-launch append are visible from here
+  // the pool rows appended by a preceding dependent-launch append are visible
+  // from here (a row that appends itself reads nothing that launch writes)
+  if (!own_row) griddep_wait();
   if (lane == 0 && !unit_bad) {
     const int first = min(NST, nstage);
     for (int n = 0; n < first; ++n) mma_issue_stage(p, hdr, ring, n, n, t_begin, t_end, j0, h, lg_p);
+  }
+  if (append_here) {  // the row's own K/V, converted, to the pool (and below to the stage)
+    uint32_t raw[4] = {kw[0], kw[1], kw[2], kw[3]};
+    convert_new<KV_E4M3, 4>(p, h, false, raw, kw);
+    raw[0] = vw[0]; raw[1] = vw[1]; raw[2] = vw[2]; raw[3] = vw[3];
+    convert_new<KV_E4M3, 4>(p, h, true, raw, vw);
+    const int pid = hdr->pid[(pos >> lg_p) - j0];
+    if (pid >= 0 && pid < p.num_pages) {
+      store_piece<4>(pool_elem(p.k_pool, p, pid, h, pos & (P - 1), 4 * lane, 1), kw);
+      store_piece<4>(pool_elem(p.v_pool, p, pid, h, pos & (P - 1), 4 * lane, 1), vw);
+    }
   }
 
   // ---- query fragments (B of Q.K), f16, in the permuted k order of the K fragments:
@@ -294,6 +317,12 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
     }
     unsigned char* ks = ring + static_cast<size_t>(s) * kMmaStageBytes;
     unsigned char* vs = ks + ST * 128;
+    if (append_here && n == nstage - 1) {  // the row's own slot, as appended: lane l's 4 bytes
+      const int r = pos - (t_begin + n * ST);  // sit in 16-byte chunk l / 4 of the swizzled row
+      store_piece<4>(ks + sw128(r, lane >> 2) + 4 * (lane & 3), kw);
+      store_piece<4>(vs + sw128(r, lane >> 2) + 4 * (lane & 3), vw);
+      __syncwarp();
+    }
     const int n_valid = min(ST, t_end - (t_begin + n * ST));  // 1..32
     const bool full = n_valid == ST;
     // ---- S^T = K . Q^T for the stage's two 16-key m-tiles; the two k halves

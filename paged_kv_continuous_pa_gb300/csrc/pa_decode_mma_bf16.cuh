@@ -102,6 +102,15 @@ __device__ __forceinline__ void decode_unit_mma_bf16(const AttnParams& p, int un
       qf[kb][1] = g4 < G ? __ldg(qs + 8 * kb + 4 + t4) : 0u;
     }
   }
+  // a row that appends itself (pa_step): lane l loads elements 4l .. 4l+3 of
+  // its new K and V before anything else, so that they have landed by the
+  // time the page ids have
+  const bool own_row = row_appends_itself(p, row);
+  uint32_t kw[4], vw[4];
+  if (own_row) {
+    load_new_raw<4>(p, row, h, 4 * lane, false, kw);
+    load_new_raw<4>(p, row, h, 4 * lane, true, vw);
+  }
   const int seq = __ldg(p.seq_ids + row);
   const int pos = __ldg(p.positions + row);
   const int P = p.P;
@@ -122,6 +131,7 @@ __device__ __forceinline__ void decode_unit_mma_bf16(const AttnParams& p, int un
   const int npg = (t_end + P - 1) / P - j0;
   const int nstage = (t_end - t_begin + ST - 1) / ST;
   const int lg_p = 31 - __clz(P);
+  const bool append_here = own_row && split == nsplit - 1;
 
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   MmaSmemHeader* hdr = reinterpret_cast<MmaSmemHeader*>(smem);
@@ -150,10 +160,23 @@ __device__ __forceinline__ void decode_unit_mma_bf16(const AttnParams& p, int un
       record_error(p.status, ST_OUT_OF_RANGE);
     }
   }
-  griddep_wait();  // the pool rows appended by a preceding dependent-launch append are visible from here
+  // the pool rows appended by a preceding dependent-launch append are visible
+  // from here (a row that appends itself reads nothing that launch writes)
+  if (!own_row) griddep_wait();
   if (lane == 0 && !unit_bad) {
     const int first = min(NST, nstage);
     for (int n = 0; n < first; ++n) mma_bf_issue_stage(p, hdr, ring, n, n, t_begin, t_end, j0, h, lg_p);
+  }
+  if (append_here) {  // the row's own K/V, converted, to the pool (and below to the stage)
+    uint32_t raw[4] = {kw[0], kw[1], kw[2], kw[3]};
+    convert_new<KV_BF16, 4>(p, h, false, raw, kw);
+    raw[0] = vw[0]; raw[1] = vw[1]; raw[2] = vw[2]; raw[3] = vw[3];
+    convert_new<KV_BF16, 4>(p, h, true, raw, vw);
+    const int pid = hdr->pid[(pos >> lg_p) - j0];
+    if (pid >= 0 && pid < p.num_pages) {
+      store_piece<8>(pool_elem(p.k_pool, p, pid, h, pos & (P - 1), 4 * lane, 2), kw);
+      store_piece<8>(pool_elem(p.v_pool, p, pid, h, pos & (P - 1), 4 * lane, 2), vw);
+    }
   }
   const float score_scale = p.qk_scale_log2_h[PA_HEAD(p, h)];
 
@@ -194,6 +217,13 @@ __device__ __forceinline__ void decode_unit_mma_bf16(const AttnParams& p, int un
     }
     unsigned char* st = ring + static_cast<size_t>(s) * kBfStageBytes;
     unsigned char* vs = st + 2 * kBfHalfBytes;
+    if (append_here && n == nstage - 1) {  // the row's own slot, as appended: lane l's 8 bytes
+      const int r = pos - (t_begin + n * ST);  // sit in half l / 16, 16-byte chunk (l % 16) / 2
+      const uint32_t off = (lane >> 4) * kBfHalfBytes + sw128(r, (lane & 15) >> 1) + 8 * (lane & 1);
+      store_piece<8>(st + off, kw);
+      store_piece<8>(vs + off, vw);
+      __syncwarp();
+    }
     const int n_valid = min(ST, t_end - (t_begin + n * ST));  // 1..32
     const bool full = n_valid == ST;
     // ---- S^T = K . Q^T, even and odd head blocks in separate accumulators

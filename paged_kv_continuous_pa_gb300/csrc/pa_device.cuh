@@ -161,6 +161,16 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// The K/V append's encoders (one definition for the append kernel and the
+// attention units that append their own rows): fp32 -> bf16 round to nearest
+// even; fp32 -> e4m3 as satfinite round-to-nearest-even of x / scale with one
+// IEEE binary32 division.
+__device__ __forceinline__ uint32_t encode_bf16(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+
+__device__ __forceinline__ uint32_t encode_e4m3(float x, float scale) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3)) & 0xffu;
+}
+
 // Two e4m3 codes in the low 16 bits -> two floats, exactly (every e4m3 value is
 // an f16 value), through the hardware e4m3x2 -> f16x2 conversion.
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {

@@ -65,6 +65,13 @@ struct AppendParams {
   int32_t head_scales;  // 1: k_scale_h / v_scale_h hold one scale per kv head; 0: entry 0 holds the per-tensor scale
   float k_scale_h[kMaxHeadScales], v_scale_h[kMaxHeadScales];
   int32_t* status;
+  // 0: rows 0 .. n_rows-1.  Otherwise only the rows of these ranges (the
+  // chunks of a pa_step whose other rows append inside the attention units):
+  // range k is rows range_begin[k] .. + range_rows[k] - 1, and range_first[k]
+  // is the number of rows in the ranges before it.
+  int32_t n_ranges;
+  int32_t range_begin[kMaxChunks];
+  int32_t range_first[kMaxChunks + 1];
 };
 
 struct AttnParams {
@@ -104,6 +111,18 @@ struct AttnParams {
   int32_t* ws_tile_count;                 // [tiles] finished-split counters, zero between calls
   float sm_scale_log2;                    // softmax scale * log2(e) for the tile path
   int32_t dependent;                      // host: launch as a programmatic dependent of the append
+  // pa_step: every row outside the caller's chunks appends its own new K/V
+  // row inside the attention launch (the unit of its last split, per kv
+  // head), with the encoder of the append kernel; chunk rows were appended
+  // by the launch this one depends on.
+  int32_t fuse_append;
+  int32_t in_dtype;                       // KV_F32 or KV_BF16: dtype of k_new / v_new
+  const void* k_new;                      // [n_rows][Hkv][D]
+  const void* v_new;
+  float k_enc_scale_h[kMaxHeadScales];    // fp8 key scale (stored code = e4m3(x / scale)), 1 otherwise
+  int32_t n_all_chunks;                   // every chunk the caller listed (tile path or not)
+  int32_t all_chunk_begin[kMaxChunks];
+  int32_t all_chunk_end[kMaxChunks];
   CUtensorMap kmap;                       // bf16 K pool as [num_pages * Hkv * P][D], box 64 x P, 128B swizzle;
                                           // e4m3 pool (D = 128): bytes [num_pages * Hkv * P][128], box 128 x min(P, 32)
   CUtensorMap vmap;                       // V pool, same geometry

@@ -170,6 +170,61 @@ def test_fp8_encoder_matches_oracle_on_float_sweep():
     np.testing.assert_array_equal(got, ref)
 
 
+def _oracle_codes(bits_lo: int, n: int, threads: int) -> np.ndarray:
+    """The oracle's e4m3 codes of the binary32 patterns bits_lo .. bits_lo + n - 1,
+    encoded in pieces on the host cores."""
+    import concurrent.futures as cf
+    x = np.arange(bits_lo, bits_lo + n, dtype=np.uint32).view(np.float32)
+    out = np.empty(n, dtype=np.uint8)
+    piece = (n + threads - 1) // threads
+
+    def enc(i):
+        a, b = i * piece, min(n, (i + 1) * piece)
+        if a < b:
+            out[a:b] = oracle.e4m3_from_f32_array(x[a:b])
+
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(enc, range(threads)))
+    return out
+
+
+def test_fp8_append_encoder_on_every_binary32_pattern():
+    """pa_append_kv into an e4m3 pool with scale 1 (x / 1 = x) on all 2^32
+    binary32 patterns -- NaNs, infinities, subnormals and both zeros
+    included -- against the oracle's encoder, code for code.  2^26 patterns
+    per call as the K rows and the next 2^26 as the V rows; one sequence of
+    8192 positions, 64 kv heads x 128 elements, 256-token pages."""
+    n, Hkv, D, P = 1 << 26, 64, 128, 256
+    rows = n // (Hkv * D)
+    pages = rows // P
+    kp = torch.zeros((pages, Hkv, P, D), dtype=torch.uint8, device="cuda")
+    vp = torch.zeros_like(kp)
+    pool = pa.Pool(kp, vp, 1.0, 1.0)
+    bt = torch.arange(pages, dtype=torch.int32, device="cuda").reshape(1, pages)
+    seq = torch.zeros(rows, dtype=torch.int32, device="cuda")
+    pos = torch.arange(rows, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    threads = oracle.host_cores()
+
+    def patterns(lo):
+        b = torch.arange(lo, lo + n, dtype=torch.int64, device="cuda")
+        b = torch.where(b >= 1 << 31, b - (1 << 32), b).to(torch.int32)
+        return b.view(torch.float32).reshape(rows, Hkv, D)
+
+    for lo in range(0, 1 << 32, 2 * n):
+        pa.append_kv(pool, patterns(lo), patterns(lo + n), seq, pos, bt, status=status)
+        # [page][head][slot][d] -> [row = page * P + slot][head][d]: the input order
+        got_k = kp.permute(0, 2, 1, 3).reshape(-1).cpu().numpy()
+        got_v = vp.permute(0, 2, 1, 3).reshape(-1).cpu().numpy()
+        assert int(status.item()) == 0
+        for got, base in ((got_k, lo), (got_v, lo + n)):
+            ref = _oracle_codes(base, n, threads)
+            if not np.array_equal(got, ref):
+                i = int(np.flatnonzero(got != ref)[0])
+                raise AssertionError(f"pattern {base + i:#010x}: GPU code {got[i]:#04x}, oracle {ref[i]:#04x} "
+                                     f"({int(np.count_nonzero(got != ref))} of {n} differ in this piece)")
+
+
 # ------------------------------------------------------------ full sizes ----
 
 def _sampled(wl, rows, what):
