@@ -19,15 +19,16 @@
 // launch without lowering the decode occupancy.  Shared memory holds two key
 // tiles and one value tile (128-byte swizzled, loaded by 2-D tensor-map copies
 // of one page x 64 head elements each; no multicast) and the page ids of the
-// CTA's key range, read from the block table once.  Tensor memory holds three
-// S buffers (S of key tile j, then P of key tile j in place, in buffer j % 3),
-// Q and O.  Thread m owns TMEM lane m = tile row m; thread 0 alone issues
-// copies and MMAs.  Schedule of key tile j: S(j) is done -> the key buffer it
-// read takes K(j+2) and S(j+1) is issued at once (its key tile landed during
-// the previous key tile), so the next scores are ready before this softmax
-// ends; during the softmax thread 0 polls for P.V(j-1) to leave the value
-// buffer and then loads V(j); P.V(j) follows the softmax.  Every barrier has
-// at most one phase outstanding; every wait is bounded.
+// CTA's key range, read from the block table once.  Tensor memory (256
+// columns, so that two tile CTAs share an SM and one's softmax overlaps the
+// other's MMAs) holds S of the current key tile, then P of it in place, Q and
+// O.  Thread m owns TMEM lane m = tile row m; thread 0 alone issues copies and
+// MMAs.  Schedule of key tile j: P.V(j-1) done -> V(j) into the value buffer,
+// S(j) issued (K(j) landed a key tile earlier) -> S(j) done: its key buffer
+// takes K(j+2) -> softmax, one read of the 64 scores from tensor memory ->
+// P.V(j).  A tile's key range is split across CTAs in fixed pieces of
+// kTileSplitKeys keys, merged in ascending order.  Every barrier has at most
+// one phase outstanding; every wait is bounded.
 //
 // Precision: the scores and the softmax are FP32.  Each weight p enters the
 // P.V product as hi = bf16(p) and lo = bf16(p - hi), so the product sees p to
@@ -62,21 +63,22 @@ enum {
   BAR_K0 = 0,   // key buffer 0 / 1 landed
   BAR_K1 = 1,
   BAR_V = 2,    // value tile landed
-  BAR_S0 = 3,   // S of key tile j done, on BAR_S0 + j % 3
-  BAR_O = 6,    // P.V of a key tile done
-  BAR_STALL = 7,
-  BAR_COUNT = 8
+  BAR_S = 3,    // S of the current key tile done
+  BAR_O = 4,    // P.V of a key tile done
+  BAR_STALL = 5,
+  BAR_COUNT = 6
 };
 
-// TMEM columns: S / P of key tile j in buffer j % 3 at 64 * (j % 3) (P of keys
-// 32h .. 32h+31: hi in columns 32h .. 32h+15 of the buffer, lo in the 16 after
-// them); Q in [192, 192 + D/2); O in [256, 256 + D).
+// TMEM columns: S of the current key tile in [0, 64), then P of it in place
+// (keys 32h .. 32h+31: hi in columns 32h .. 32h+15, lo in the 16 after them);
+// Q in [64, 64 + D/2); O in [128, 128 + D).  256 columns: two tile CTAs fit on
+// an SM, so that one's softmax runs while the other's MMAs do.
 template <int D>
 struct PrefillTmem {
-  static constexpr uint32_t S = 0;  // buffer b at S + 64 * b
-  static constexpr uint32_t Q = 192;
-  static constexpr uint32_t O = 256;
-  static constexpr uint32_t COLS = 512;  // a power of two
+  static constexpr uint32_t S = 0;
+  static constexpr uint32_t Q = 64;
+  static constexpr uint32_t O = 128;
+  static constexpr uint32_t COLS = 256;  // a power of two
   static_assert(O >= Q + D / 2 && O + D <= COLS, "tensor memory columns overlap");
 };
 
@@ -239,84 +241,66 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
 
   constexpr uint32_t id_qk = tc::idesc_bf16_f32(kTileM, kTileN, false);
   constexpr uint32_t id_pv = tc::idesc_bf16_f32(kTileM, D, true);
-  // S(j) = Q K(j)^T into S buffer j % 3 from key buffer j % 2 (thread 0; K(j) has landed)
+  // S(j) = Q K(j)^T into the S columns from key buffer j % 2 (thread 0; K(j) has landed)
   auto issue_qk = [&](int j) {
-    const uint32_t d = tb + T::S + 64u * static_cast<uint32_t>(j % 3);
     const unsigned char* K = Ks + (j & 1) * S::TILE;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const unsigned char* kb = K + (kk / 4) * S::KH + (kk % 4) * 32;
-      tc::mma_bf16_ts(d, tb + T::Q + kk * 8, tc::smem_desc(kb, 16, 1024), id_qk, kk > 0);
+      tc::mma_bf16_ts(tb + T::S, tb + T::Q + kk * 8, tc::smem_desc(kb, 16, 1024), id_qk, kk > 0);
     }
-    tc::mma_commit(&bar[BAR_S0 + j % 3]);
+    tc::mma_commit(&bar[BAR_S]);
   };
-  // O += P(j) V(j), P as (hi, lo) from S buffer j % 3
+  // O += P(j) V(j), P as (hi, lo) from the S columns
   auto issue_pv = [&](int j) {
-    const uint32_t a = tb + T::S + 64u * static_cast<uint32_t>(j % 3);
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
       const uint64_t vb = tc::smem_desc(Vs + kk * 2048, S::KH, 1024);  // 16 keys of the MN-major value tile
-      const uint32_t ph = a + (kk / 2) * 32 + (kk % 2) * 8;            // hi of keys 16kk .. 16kk+15; lo 16 columns on
+      const uint32_t ph = tb + T::S + (kk / 2) * 32 + (kk % 2) * 8;   // hi of keys 16kk .. 16kk+15; lo 16 columns on
       tc::mma_bf16_ts(tb + T::O, ph, vb, id_pv, j > 0 || kk > 0);
       tc::mma_bf16_ts(tb + T::O, ph + 16, vb, id_pv, true);
     }
     tc::mma_commit(&bar[BAR_O]);
   };
 
+  // Key tile j: P.V(j-1) done (it has left the S columns and the value buffer)
+  // -> V(j) into the value buffer, S(j) -> softmax -> P.V(j).  Every barrier has
+  // at most one phase outstanding; every wait is bounded.
   float m_ref = -INFINITY, l_run = 0.0f;
   bool ok = !(p.debug_stall && nk > 0) || mbar_wait(&bar[BAR_STALL], 0, p.wait_limit);  // the stall runs out
   // thread 0's own waits; a failure there reaches the others through the next
   // collective wait (theirs then runs out too: bounded)
   bool issuer_ok = true;
-  if (tid == 0 && ok && nk > 0) {
-    issuer_ok = mbar_wait(&bar[BAR_K0], 0, p.wait_limit);
-    if (issuer_ok) {
-      log.seen(BAR_K0);
-      tc::fence_after_sync();
-      issue_qk(0);
-      log.issue(BAR_S0);
-    }
-  }
-  ok = __syncthreads_and(ok && issuer_ok);
+  const uint32_t col_s = tb + lane_base + T::S;
   for (int j = 0; j < nk && ok; ++j) {
-    const int sb = j % 3;
-    const uint32_t col_s = tb + lane_base + T::S + 64u * static_cast<uint32_t>(sb);
+    if (tid == 0 && issuer_ok) {
+      if (j > 0) {
+        issuer_ok = mbar_wait(&bar[BAR_O], (j - 1) & 1, p.wait_limit);
+        if (issuer_ok) {
+          log.seen(BAR_O);
+          prefill_load_kv<D>(p, &p.vmap, Vs, &bar[BAR_V], pids, jp0, j_begin + j, h, fallback_pid);
+          log.issue(BAR_V);
+        }
+      }
+      if (issuer_ok) issuer_ok = mbar_wait(&bar[BAR_K0 + (j & 1)], (j >> 1) & 1, p.wait_limit);
+      if (issuer_ok) {
+        log.seen(BAR_K0 + (j & 1));
+        tc::fence_after_sync();
+        issue_qk(j);
+        log.issue(BAR_S);
+      }
+    }
     // ---- S(j) done
-    if (!(ok = __syncthreads_and(issuer_ok && mbar_wait(&bar[BAR_S0 + sb], (j / 3) & 1, p.wait_limit)))) break;
+    if (!(ok = __syncthreads_and(issuer_ok && mbar_wait(&bar[BAR_S], j & 1, p.wait_limit)))) break;
     tc::fence_after_sync();
-    bool v_issued = j == 0;  // V(0) came with the first copies
     if (tid == 0) {
-      log.seen(BAR_S0 + sb);
+      log.seen(BAR_S);
       if (j + 2 < nk) {  // S(j) has read key buffer j % 2: refill it
         prefill_load_kv<D>(p, &p.kmap, Ks + (j & 1) * S::TILE, &bar[BAR_K0 + (j & 1)], pids, jp0, j_begin + j + 2, h,
                            fallback_pid);
         log.issue(BAR_K0 + (j & 1));
       }
-      if (j + 1 < nk) {
-        // S(j+1) now: its key tile was loaded a key tile ago, and its S buffer's
-        // last reader, P.V(j-2), was seen done before V(j-1) was loaded
-        issuer_ok = mbar_wait(&bar[BAR_K0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1, p.wait_limit);
-        if (issuer_ok) {
-          log.seen(BAR_K0 + ((j + 1) & 1));
-          tc::fence_after_sync();
-          issue_qk(j + 1);
-          log.issue(BAR_S0 + (j + 1) % 3);
-        }
-      }
     }
-    // thread 0: V(j) into the value buffer once P.V(j-1) has left it
-    auto load_v = [&](bool block) {
-      if (v_issued || !issuer_ok) return;
-      const bool done = block ? mbar_wait(&bar[BAR_O], (j - 1) & 1, p.wait_limit) : mbar_test(&bar[BAR_O], (j - 1) & 1);
-      if (!done) {
-        if (block) issuer_ok = false;
-        return;
-      }
-      log.seen(BAR_O);
-      prefill_load_kv<D>(p, &p.vmap, Vs, &bar[BAR_V], pids, jp0, j_begin + j, h, fallback_pid);
-      log.issue(BAR_V);
-      v_issued = true;
-    };
     // ---- online softmax of this row's 64 scores (log2 domain), in two halves of
     // 32 read from tensor memory twice (for the maximum, then for the weights),
     // so that no more than 32 scores are live in registers
@@ -325,19 +309,18 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
     float mx = -INFINITY;
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
-      float s[32];
-      tc::tmem_ld32(col_s + 32 * half, s);
+      float sc[32];
+      tc::tmem_ld32(col_s + 32 * half, sc);
       if (edge) {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          if (key0 + 32 * half + i > my_pos) s[i] = -INFINITY;
+          if (key0 + 32 * half + i > my_pos) sc[i] = -INFINITY;
       }
-      float mx4[4] = {s[0], s[1], s[2], s[3]};
+      float mx4[4] = {sc[0], sc[1], sc[2], sc[3]};
 #pragma unroll
-      for (int i = 4; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+      for (int i = 4; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], sc[i]);
       mx = fmaxf(mx, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])));
     }
-    if (tid == 0) load_v(false);
     mx = __fmul_rn(mx, p.sm_scale_log2);  // the scale is positive: the largest scaled score is the scaled largest one
     float alpha = 1.0f;
     if (mx > __fadd_rn(m_ref, kRescaleSlack)) {
@@ -347,25 +330,25 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
     }
     // every score so far masked: the weights are ex2(-inf) = 0 against any finite reference
     const float neg_ref = m_ref == -INFINITY ? 0.0f : -m_ref;
-    // weights -> (hi, lo) bf16 pairs in place of S: keys 32h .. 32h+31 of the
-    // buffer's half h as hi in its first 16 columns and lo in the next 16
+    // weights -> (hi, lo) bf16 pairs in place of S: keys 32h .. 32h+31 as hi
+    // in columns 32h .. 32h+15 and lo in the 16 after them
     float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
-      float s[32];
-      tc::tmem_ld32(col_s + 32 * half, s);
+      float sc[32];
+      tc::tmem_ld32(col_s + 32 * half, sc);
       if (edge) {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          if (key0 + 32 * half + i > my_pos) s[i] = -INFINITY;
+          if (key0 + 32 * half + i > my_pos) sc[i] = -INFINITY;
       }
 #pragma unroll
       for (int q8 = 0; q8 < 2; ++q8) {
         uint32_t hw[8], lw[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float a = ex2(fmaf(s[16 * q8 + 2 * i], p.sm_scale_log2, neg_ref));
-          const float c = ex2(fmaf(s[16 * q8 + 2 * i + 1], p.sm_scale_log2, neg_ref));
+          const float a = ex2(fmaf(sc[16 * q8 + 2 * i], p.sm_scale_log2, neg_ref));
+          const float c = ex2(fmaf(sc[16 * q8 + 2 * i + 1], p.sm_scale_log2, neg_ref));
           ls[i] = __fadd_rn(ls[i], __fadd_rn(a, c));
           const __nv_bfloat162 hi = __floats2bfloat162_rn(a, c);
           const __nv_bfloat162 lo = __floats2bfloat162_rn(__fsub_rn(a, __low2float(hi)), __fsub_rn(c, __high2float(hi)));
@@ -375,13 +358,13 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
         tc::tmem_st8(col_s + 32 * half + q8 * 8, hw);
         tc::tmem_st8(col_s + 32 * half + 16 + q8 * 8, lw);
       }
-      if (tid == 0) load_v(false);
     }
     const float lsum = __fadd_rn(__fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3])),
                                  __fadd_rn(__fadd_rn(ls[4], ls[5]), __fadd_rn(ls[6], ls[7])));
     l_run = __fadd_rn(l_run, lsum);
     if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-      // the reference max moved: rescale O once P.V(j-1) has finished writing it
+      // the reference max moved: rescale O (P.V(j-1), its last writer, is done:
+      // thread 0 saw it before issuing S(j); the others see it here)
       if (mbar_wait(&bar[BAR_O], (j - 1) & 1, p.wait_limit)) {
         tc::fence_after_sync();
 #pragma unroll 1
@@ -397,7 +380,6 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
       }
     }
     tc::tmem_wait_st();
-    if (tid == 0) load_v(true);
     // ---- value tile: keys past the chunk's last position may hold stale or
     // poisoned values; zero those rows so that 0-weights never meet a NaN
     if (!(ok = __syncthreads_and(ok && issuer_ok && mbar_wait(&bar[BAR_V], j & 1, p.wait_limit)))) break;
@@ -491,18 +473,21 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
         // Merge in ascending key-range order.  Each row's weights f[row][sp] and
         // 1 / sum go to shared memory (the K/V buffers are free now); then all
         // threads sweep the tile in 16-byte pieces (thread t: pieces t, t + 128,
-        // ...; a row's pieces are consecutive), eight pieces and two key ranges
-        // of loads in flight at a time.
+        // ...; a row's pieces are consecutive), eight loads in flight a thread
+        // (four pieces, two key ranges): the merge is bound by the loads one SM
+        // keeps in flight.
         float* ftab = reinterpret_cast<float*>(sm);  // [kTileM][nsplit], then [kTileM] inverse sums
         const bool fits = (kTileM * (nsplit + 1)) * 4 <= S::BAR_OFF;
         if (fits) {
           float M = -INFINITY;
-          for (int sp = 0; sp < nsplit; ++sp) {
+#pragma unroll 4
+          for (int sp = 0; sp < nsplit; ++sp) {  // independent loads, several in flight
             const float mv = row_valid ? __ldcg(p.ws_tile_ml + (slot0 + sp) * 2) : 0.0f;
             ftab[m * nsplit + sp] = mv;
             M = fmaxf(M, mv);
           }
           float lsum = 0.0f;
+#pragma unroll 4
           for (int sp = 0; sp < nsplit; ++sp) {
             const float f = ex2(__fsub_rn(ftab[m * nsplit + sp], M));
             ftab[m * nsplit + sp] = f;
