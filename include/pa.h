@@ -225,7 +225,7 @@ pa_status pa_attention_noalloc(const pa_pool *pool, int32_t n_rows, const void *
 /* Split-KV chunk length in tokens: a row at position p is cut into
  * ceil((p + 1) / split) pieces merged in ascending order.  A process-wide
  * constant (default 4096), a multiple of 64 up to 4096, never derived from the batch.
- * These settings (split length, wait limit, injected stall) may be changed from
+ * These settings (split length, row groups, wait limit, injected stall) may be changed from
  * any thread; a call reads each of them once, when it starts, so one call never
  * mixes two values.  A workspace sized by pa_attention_workspace_bytes before a
  * change may be too small after it: the call then returns PA_ERR_INVALID_ARG.
@@ -233,6 +233,23 @@ pa_status pa_attention_noalloc(const pa_pool *pool, int32_t n_rows, const void *
  * Returns PA_ERR_INVALID_ARG for a value that is not a positive multiple of 64. */
 pa_status pa_set_split_tokens(int32_t tokens);
 int32_t pa_get_split_tokens(void);
+
+/* Row groups for the FP8 (E4M3) tensor-core decode units (head_dim 128, bf16
+ * queries): with rows = 2, 4 or 8, one CTA takes that many consecutive decode
+ * rows of the call for one kv head and split, and the leading pages that all
+ * of its rows share (the same physical page ids, full 32-token stages, none a
+ * row's last) are copied into shared memory once and read by every row
+ * ("GPU inference engine engineering", section "The same bits in any batch":
+ * a shared prompt prefix staged once for eight rows).  Rows share pages only
+ * when the caller lists the rows of one prefix next to one another (a
+ * scheduler that groups its batches by prefix, section "Caching measured on
+ * the real prompt structure").  1 (the default) runs one row per CTA.  Output
+ * bits never depend on it: each row's arithmetic is the same in both forms.
+ * Other pools and query dtypes ignore it.  A process-wide setting, read once
+ * per call like the split length.  Returns PA_ERR_INVALID_ARG for a value
+ * other than 1, 2, 4 or 8. */
+pa_status pa_set_row_groups(int32_t rows);
+int32_t pa_get_row_groups(void);
 
 /* Longest time, in microseconds, one device-side wait (for a copy or an MMA
  * to complete) may take before it gives up with PA_ERR_TIMEOUT; 0 restores

@@ -103,6 +103,10 @@ def load(path: str = LIB_PATH):
         L.pa_set_split_tokens.restype = st
         L.pa_get_split_tokens.argtypes = []
         L.pa_get_split_tokens.restype = i32
+        L.pa_set_row_groups.argtypes = [i32]
+        L.pa_set_row_groups.restype = st
+        L.pa_get_row_groups.argtypes = []
+        L.pa_get_row_groups.restype = i32
         L.pa_set_wait_limit.argtypes = [ctypes.c_uint32]
         L.pa_set_wait_limit.restype = None
         L.pa_debug_stall_waits.argtypes = [i32]
@@ -359,6 +363,14 @@ def set_split_tokens(tokens: int):
 
 def get_split_tokens() -> int:
     return int(load().pa_get_split_tokens())
+
+
+def set_row_groups(rows: int):
+    _check(load().pa_set_row_groups(int(rows)))
+
+
+def get_row_groups() -> int:
+    return int(load().pa_get_row_groups())
 
 
 def set_wait_limit(microseconds: int):

@@ -39,6 +39,7 @@ namespace {
 thread_local char g_last_error[512] = "";
 // process-wide settings; any thread may change them, and a call reads each once
 std::atomic<int32_t> g_split_tokens{pa::kDefaultSplitTokens};
+std::atomic<int32_t> g_row_groups{1};
 std::atomic<uint32_t> g_wait_limit{pa::kDefaultWaitLimit};
 std::atomic<int32_t> g_debug_stall{0};
 
@@ -348,6 +349,7 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
   p.q_is_bf16 = q_dtype == PA_BF16;
   p.split_tokens = split_tokens;
   p.max_splits = pl.max_splits;
+  p.row_group = g_row_groups.load(std::memory_order_relaxed);
   // per kv head (or entry 0 for all): softmax scale * k scale * log2(e), and the v scale
   p.head_scales = pool->head_scales ? 1 : 0;
   for (int h = 0; h < (pool->head_scales ? d.num_kv_heads : 1); ++h) {
@@ -595,6 +597,15 @@ pa_status pa_set_split_tokens(int32_t tokens) {
 }
 
 int32_t pa_get_split_tokens(void) { return g_split_tokens.load(std::memory_order_relaxed); }
+
+pa_status pa_set_row_groups(int32_t rows) {
+  if (rows != 1 && rows != 2 && rows != 4 && rows != 8)
+    return fail(PA_ERR_INVALID_ARG, "row groups %d is not 1, 2, 4 or 8", rows);
+  g_row_groups.store(rows, std::memory_order_relaxed);
+  return PA_OK;
+}
+
+int32_t pa_get_row_groups(void) { return g_row_groups.load(std::memory_order_relaxed); }
 
 void pa_set_wait_limit(uint32_t microseconds) {
   g_wait_limit.store(microseconds == 0 ? pa::kDefaultWaitLimit : microseconds, std::memory_order_relaxed);

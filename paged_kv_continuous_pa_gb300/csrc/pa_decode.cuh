@@ -505,7 +505,7 @@ template <int D, int G, int KVT, int NW, int THREADS>
 __device__ __forceinline__ void decode_finish(const AttnParams& p, bool bad, int32_t* last_flag, float* red_acc,
                                               const float* red_ml, size_t out_row, int row, int h, int split,
                                               int nsplit, bool q_bf16, int ring_bytes) {
-  const int tid = threadIdx.x;
+  const int tid = static_cast<int>(threadIdx.x) % THREADS;  // a warp of a wider CTA runs it as its own
   if (nsplit == 1) {
     for (int i = tid; i < G * D; i += THREADS) {
       const int g = i / D, d = i % D;

@@ -129,9 +129,14 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 
 // Barrier over the first NT threads of the CTA (named barrier 1), for code
 // that runs in a CTA whose remaining warps have other work or have exited.
+// A single warp (NT = 32) syncs on its own, so that code written for a
+// one-warp CTA also runs in each warp of a wider one.
 template <int NT>
 __device__ __forceinline__ void sync_threads_n() {
-  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+  if constexpr (NT == 32)
+    __syncwarp();
+  else
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
 // Programmatic dependent launch.  A kernel launched as a dependent of the

@@ -111,6 +111,7 @@ struct AttnParams {
   int32_t* ws_tile_count;                 // [tiles] finished-split counters, zero between calls
   float sm_scale_log2;                    // softmax scale * log2(e) for the tile path
   int32_t dependent;                      // host: launch as a programmatic dependent of the append
+  int32_t row_group;                      // e4m3 tensor-core decode: rows per CTA (1, 2, 4 or 8)
   // pa_step: every row outside the caller's chunks appends its own new K/V
   // row inside the attention launch (the unit of its last split, per kv
   // head), with the encoder of the append kernel; chunk rows were appended

@@ -131,6 +131,19 @@ def test_split_tokens_setting(lib):
         lib.pa_set_split_tokens(old)
 
 
+def test_row_groups_setting(lib):
+    old = lib.pa_get_row_groups()
+    assert old == 1  # one row per CTA unless the caller asks
+    try:
+        for bad in (0, 3, 5, 16, -2):
+            assert lib.pa_set_row_groups(bad) == pa.PA_ERR_INVALID_ARG
+            assert lib.pa_get_row_groups() == old
+        for rows in (2, 4, 8, 1):
+            assert lib.pa_set_row_groups(rows) == pa.PA_OK and lib.pa_get_row_groups() == rows
+    finally:
+        lib.pa_set_row_groups(old)
+
+
 def test_settings_change_from_other_threads(lib):
     """One thread flips the split length while others size workspaces: every
     answer is the one of the two settings, never a mix (a call reads it once)."""

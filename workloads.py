@@ -21,7 +21,7 @@ from __future__ import annotations
 import concurrent.futures as cf
 import math
 import os
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 
 import numpy as np
 
@@ -319,12 +319,13 @@ def mixed_step(seed: int = 3, n_decode: int = 256, ctx_lo: int = 64, ctx_hi: int
 
 
 def shared_prefix(seed: int = 4, n_seqs: int = 768, share_frac: float = 0.7, prefix: int = 90,
-                  prompt: int = 128, max_gen: int = 128) -> Workload:
+                  prompt: int = 128, max_gen: int = 128, P: int = 32, Hq: int = 28, Hkv: int = 4) -> Workload:
     """n_seqs sequences at position prompt + g, g ~ U{0..max_gen-1}; a fraction
-    share_frac of them share a `prefix`-token prefix whose full 32-token pages
-    are physically shared; Hq 28 / Hkv 4, D 128, fp8 e4m3 K/V (bf16 rows in),
-    bf16 Q, P 32.  The page that holds the prefix's tail is a private copy."""
-    P, Hq, Hkv, D = 32, 28, 4, 128
+    share_frac of them share a `prefix`-token prefix whose full pages are
+    physically shared; Hq 28 / Hkv 4, D 128, fp8 e4m3 K/V (bf16 rows in),
+    bf16 Q, P 32 by default.  The page that holds the prefix's tail is a
+    private copy."""
+    D = 128
     rng = np.random.Generator(np.random.PCG64(seed))
     g = rng.integers(0, max_gen, size=n_seqs)
     ctx = (prompt + g + 1).astype(np.int64)  # keys attended by each decode row
@@ -396,9 +397,33 @@ def shared_prefix(seed: int = 4, n_seqs: int = 768, share_frac: float = 0.7, pre
                     hist_pos=hist_pos, hist_k=hist_k, hist_v=hist_v, seq_ids=seq_ids,
                     positions=positions, q=q, k_new=k_new, v_new=v_new, k_scale=k_scale,
                     v_scale=v_scale, shared_pages=n_shared_pages if n_share > 1 else 0,
-                    description=f"7B-class shared-prefix decode: batch {n_seqs}, Hq28/Hkv4, D128, fp8 "
+                    description=f"7B-class shared-prefix decode: batch {n_seqs}, Hq{Hq}/Hkv{Hkv}, D128, fp8 "
                                 f"e4m3 K/V (per-tensor scale), bf16 Q, {prompt} prompt + U{{0..{max_gen - 1}}} "
-                                f"generated, {n_share} seqs share a {prefix}-token prefix, P32")
+                                f"generated, {n_share} seqs share a {prefix}-token prefix, P{P}")
+
+
+def reorder_rows(wl: Workload, order) -> Workload:
+    """The same decode step with its rows listed in `order` (a permutation of
+    the rows): every row keeps its sequence, position, query and new K/V."""
+    if wl.chunks:
+        raise ValueError("reorder_rows takes decode-only steps")
+    order = np.asarray(order, dtype=np.int64)
+    if sorted(order.tolist()) != list(range(wl.n_rows)):
+        raise ValueError("order is not a permutation of the rows")
+    return replace(wl, seq_ids=wl.seq_ids[order].copy(), positions=wl.positions[order].copy(),
+                   q=wl.q[order].copy(), k_new=wl.k_new[order].copy(), v_new=wl.v_new[order].copy(),
+                   name=wl.name + "_grouped", description=wl.description + "; rows grouped by prefix")
+
+
+def group_by_prefix(wl: Workload) -> Workload:
+    """The rows listed prefix by prefix, as a scheduler that groups its batches
+    by prefix would list them: rows whose sequences start on the same physical
+    page become adjacent (each group in the rows' original order), groups in
+    order of first appearance.  No row's inputs change."""
+    first = wl.block_tables[wl.seq_ids, 0]
+    _, idx_first, inv = np.unique(first, return_index=True, return_inverse=True)
+    group_rank = np.argsort(np.argsort(idx_first))  # group ordinal by first appearance
+    return reorder_rows(wl, np.argsort(group_rank[inv.reshape(-1)], kind="stable"))
 
 
 def chunked_step(seed: int, chunks, decode_ctx=(), Hq: int = 16, Hkv: int = 8, D: int = 128, P: int = 32,
