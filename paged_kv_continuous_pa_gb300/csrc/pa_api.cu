@@ -118,7 +118,8 @@ Plan make_plan(const pa_pool_desc& d, int32_t n_rows, int32_t hq, int32_t max_bl
     off += pad(slots * d.head_dim * sizeof(float));
   }
   if (pl.tile_splits > 1) {
-    const size_t slots = static_cast<size_t>(pl.total_rows) * hq * pl.tile_splits;
+    // tile-major partials: per (tile, key range) all 128 tile rows
+    const size_t slots = static_cast<size_t>(pl.total_tiles) * pl.tile_splits * pa::kTileRowsTotal;
     pl.t_count = off;
     off += pad(static_cast<size_t>(pl.total_tiles) * sizeof(int32_t));
     pl.t_ml = off;

@@ -150,6 +150,9 @@ __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("grid
 // Order this thread's generic-proxy shared-memory accesses before its later
 // async-proxy (bulk-copy) operations on shared memory.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Generic-proxy global memory accesses (another CTA's stores, ordered before
+// this point by an acquire) before this thread's bulk copies read them.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // 2^x with the hardware approximation (ex2.approx.ftz.f32: relative error
 // about 2^-22, subnormal results flushed to zero).  Softmax weights below

@@ -51,71 +51,74 @@ struct PrefillSmem {  // byte offsets from a 1024-byte aligned base
   static constexpr int NH = D / 64;        // 64-element halves of the head dim
   static constexpr int KH = kTileN * 128;  // one half of a K or V tile: 8 KiB
   static constexpr int TILE = NH * KH;     // one K or V tile
-  static constexpr int K_OFF = 0;          // two key tiles
-  static constexpr int V_OFF = K_OFF + 2 * TILE;
-  static constexpr int BAR_OFF = V_OFF + TILE;
+  static constexpr int SLOTS = 3;          // ring of key / value tiles, from offset 0
+  static constexpr int BAR_OFF = SLOTS * TILE;  // barriers, then the TMEM slot (+112) and the last-CTA flag (+116)
   static constexpr int PID_OFF = BAR_OFF + 128;
   static constexpr int TOTAL = PID_OFF + ((kTilePids * 4 + 15) / 16) * 16;
   static constexpr int BYTES = TOTAL + 1024;  // slack for aligning the base
 };
 
 enum {
-  BAR_K0 = 0,   // key buffer 0 / 1 landed
-  BAR_K1 = 1,
-  BAR_V = 2,    // value tile landed
-  BAR_S = 3,    // S of the current key tile done
-  BAR_O = 4,    // P.V of a key tile done
-  BAR_STALL = 5,
-  BAR_COUNT = 6
+  BAR_R0 = 0,     // ring slot 0 / 1 / 2 landed (a key or a value tile)
+  BAR_S0 = 3,     // S of S buffer 0 / 1 done
+  BAR_O = 5,      // P.V of a key tile done
+  BAR_STALL = 6,
+  BAR_COUNT = 7,
+  BAR_M0 = 7,     // split merge: partial block landed in ring slot 0 / 1 / 2
+  BAR_ALL = 10    // barriers initialised (the merge's are not in the issue log)
 };
+constexpr int kMergeSlots = 3;
 
-// TMEM columns: S of the current key tile in [0, 64), then P of it in place
-// (keys 32h .. 32h+31: hi in columns 32h .. 32h+15, lo in the 16 after them);
-// Q in [64, 64 + D/2); O in [128, 128 + D).  256 columns: two tile CTAs fit on
-// an SM, so that one's softmax runs while the other's MMAs do.
+// TMEM columns: two S buffers, S(j) in [64 (j % 2), 64 (j % 2) + 64), then
+// P(j) in place (keys 32h .. 32h+31: hi in columns 32h .. 32h+15, lo in the 16
+// after them); Q in [128, 128 + D/2); O in [256, 256 + D).  With two S
+// buffers S(j+1) runs on the tensor cores while the threads turn S(j) into
+// P(j), and P.V(j) while they start on S(j+1).
 template <int D>
 struct PrefillTmem {
-  static constexpr uint32_t S = 0;
-  static constexpr uint32_t Q = 64;
-  static constexpr uint32_t O = 128;
-  static constexpr uint32_t COLS = 256;  // a power of two
-  static_assert(O >= Q + D / 2 && O + D <= COLS, "tensor memory columns overlap");
+  static constexpr uint32_t S = 0;  // S buffer b at S + 64 b
+  static constexpr uint32_t Q = 128;
+  static constexpr uint32_t O = 256;
+  static constexpr uint32_t COLS = 512;  // a power of two
+  static_assert(Q >= S + 2 * kTileN && O >= Q + D / 2 && O + D <= COLS, "tensor memory columns overlap");
 };
 
-// Thread 0's record of the copies and MMAs it issued on each barrier; a barrier
-// never has more than one phase outstanding, so after a failure each pending
-// operation is drained by waiting for the parity of its own phase.
+// A role thread's record of the copies and MMAs it issued on each barrier, in
+// two bit masks (registers, not local memory): a phase outstanding, and the
+// parity of the last phase issued.  A barrier never has more than one phase
+// outstanding, so after a failure each pending operation is drained by
+// waiting for the parity of its own phase.
 struct PrefillIssueLog {
-  int issued[BAR_COUNT];
-  int observed[BAR_COUNT];
-  __device__ void issue(int b) { ++issued[b]; }
-  __device__ void seen(int b) { observed[b] = issued[b]; }
+  uint32_t pending = 0u, parity = 0u;
+  __device__ void issue(int b) {
+    parity ^= 1u << b;
+    pending |= 1u << b;
+  }
+  __device__ void seen(int b) { pending &= ~(1u << b); }
   __device__ void drain(uint64_t* bar) {
     for (int b = 0; b < BAR_COUNT; ++b)
-      if (issued[b] > observed[b]) mbar_wait(&bar[b], (issued[b] - 1) & 1, kDrainWaitLimit);
+      if ((pending >> b) & 1u) mbar_wait(&bar[b], ((parity >> b) & 1u) ^ 1u, kDrainWaitLimit);
   }
 };
 
-// Key tile j (keys 64j .. 64j+63) of kv head h into a tile buffer: one box of
-// min(P, 64) keys x 64 head elements per page piece and head-dim half.  Page
-// ids come from the CTA's table in shared memory (pids[jp - jp0]); keys past
-// the sequence read a valid page instead (masked or zeroed later).
+// Key tile j (keys 64j .. 64j+63) into a tile buffer: one box of min(P, 64)
+// keys x 64 head elements per page piece and head-dim half.  ybase[jp - jp0]
+// is the tensor-map row of page jp's first slot for this kv head (built once
+// from the block table; a page past the sequence has a valid page's row:
+// masked or zeroed later).  P = 2^lg_p.  The issuing thread reads shared
+// memory only: no kernel parameter, no division.
 template <int D>
-__device__ __forceinline__ void prefill_load_kv(const AttnParams& p, const CUtensorMap* map, unsigned char* dst,
-                                                uint64_t* bar, const int32_t* pids, int jp0, int j, int h,
-                                                int fallback_pid) {
+__device__ __forceinline__ void prefill_load_kv(const CUtensorMap* map, unsigned char* dst, uint64_t* bar,
+                                                const int32_t* ybase, int jp0, int j, int lg_p) {
   constexpr int NH = D / 64;
-  const int P = p.P;
-  const int BR = P < kTileN ? P : kTileN;  // rows of one box: a page, or a 64-key part of a larger page
+  const int lg_br = lg_p < 6 ? lg_p : 6;  // rows of one box: a page, or a 64-key part of a larger page
   mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kTileN * D * 2));
-  for (int k = 0; k < kTileN / BR; ++k) {
-    const int t = j * kTileN + k * BR;  // first key of the box
-    int pid = pids[t / P - jp0];
-    if (pid < 0 || pid >= p.num_pages) pid = fallback_pid;
-    const int y = (pid * p.Hkv + h) * P + t % P;
+  for (int k = 0; k < (kTileN >> lg_br); ++k) {
+    const int t = j * kTileN + (k << lg_br);  // first key of the box
+    const int y = ybase[(t >> lg_p) - jp0] + (t & ((1 << lg_p) - 1));
 #pragma unroll
     for (int half = 0; half < NH; ++half)
-      tc::tma_load_2d(dst + half * PrefillSmem<D>::KH + k * BR * 128, map, half * 64, y, bar);
+      tc::tma_load_2d(dst + half * PrefillSmem<D>::KH + (k << lg_br) * 128, map, half * 64, y, bar);
   }
 }
 
@@ -125,12 +128,13 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
   using T = PrefillTmem<D>;
   constexpr int NH = S::NH;
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* Ks = sm + S::K_OFF;  // key buffer b at Ks + b * TILE
-  unsigned char* Vs = sm + S::V_OFF;
+  // ring slot r at sm + r * TILE
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S::BAR_OFF);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::BAR_OFF + 64);
-  int32_t* last_flag = reinterpret_cast<int32_t*>(sm + S::BAR_OFF + 72);
-  int32_t* pids = reinterpret_cast<int32_t*>(sm + S::PID_OFF);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::BAR_OFF + 112);
+  int32_t* last_flag = reinterpret_cast<int32_t*>(sm + S::BAR_OFF + 116);
+  int32_t* last_item = reinterpret_cast<int32_t*>(sm + S::BAR_OFF + BAR_ALL * 8);  // per ring slot: last item issued
+  static_assert(BAR_ALL * 8 + S::SLOTS * 4 <= 112, "barriers overlap the TMEM slot");
+  int32_t* pids = reinterpret_cast<int32_t*>(sm + S::PID_OFF);  // page ids, then tensor-map rows
 
   int c = 0;
   while (c + 1 < p.n_chunks && cta >= p.chunk_cta_begin[c + 1]) ++c;
@@ -177,9 +181,13 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
   // allocate tensor memory first: until it has, this CTA keeps others off the SM
   if (warp == 0) tc::tmem_alloc(tslot, T::COLS);
   if (tid == 0) {
-    for (int i = 0; i < BAR_COUNT; ++i) mbar_init(&bar[i], 1);  // nothing ever arrives on BAR_STALL
+    for (int i = 0; i < BAR_ALL; ++i) mbar_init(&bar[i], 1);  // nothing ever arrives on BAR_STALL
+    for (int i = 0; i < S::SLOTS; ++i) last_item[i] = -1;
     fence_barrier_init();
+    tc::prefetch_tensormap(&p.kmap);  // the copy issuer's descriptors, fetched while the setup runs
+    tc::prefetch_tensormap(&p.vmap);
   }
+  const int lg_p = 31 - __clz(p.P);
   // the Q row (the query is the caller's input: no dependence on a preceding
   // append), then the checks: the tile's rows must be consecutive positions of
   // one sequence, the pages its keys need in range; the CTA's page ids go to
@@ -217,20 +225,38 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
   const bool run = !bad;
   if (!run && tid == 0) record_error(p.status, ST_OUT_OF_RANGE);
   const int nk = run ? nk_cta : 0;  // key tiles of this CTA
-  const int fallback_pid = run ? pids[0] : 0;
-
-  PrefillIssueLog log = {};
-  griddep_wait();  // the chunk's own rows, appended by a preceding dependent-launch append, are visible from here
-  if (tid == 0 && nk > 0) {
-    prefill_load_kv<D>(p, &p.kmap, Ks, &bar[BAR_K0], pids, jp0, j_begin, h, fallback_pid);
-    log.issue(BAR_K0);
-    prefill_load_kv<D>(p, &p.vmap, Vs, &bar[BAR_V], pids, jp0, j_begin, h, fallback_pid);
-    log.issue(BAR_V);
-    if (nk > 1) {
-      prefill_load_kv<D>(p, &p.kmap, Ks + S::TILE, &bar[BAR_K1], pids, jp0, j_begin + 1, h, fallback_pid);
-      log.issue(BAR_K1);
+  // page ids -> tensor-map rows (pages past the sequence take the first page's)
+  if (run) {
+    const int fallback_pid = __ldg(bt + jp0);  // = pids[0], read where no thread overwrites it
+    for (int jp = jp0 + tid; jp <= jp_last; jp += kTileM) {
+      int pid = pids[jp - jp0];
+      if (pid < 0 || pid >= p.num_pages) pid = fallback_pid;
+      pids[jp - jp0] = (pid * p.Hkv + h) << lg_p;
     }
   }
+  __syncthreads();
+
+  PrefillIssueLog log;
+  // ---- the ring: the three tile buffers take key and value tiles in the
+  // order the tensor pipe reads them, K(0), K(1), V(0), K(2), V(1), K(3), ...
+  // (item i in slot i % 3); a slot takes item i + 3 once the MMA that read
+  // item i is done, so a value tile is copied a key tile ahead of its P.V and
+  // a key tile about one ahead of its S.
+  auto item_tile = [](int i) { return i == 0 ? 0 : ((i & 1) ? (i + 1) / 2 : (i - 2) / 2); };
+  auto k_item = [](int jj) { return jj == 0 ? 0 : 2 * jj - 1; };
+  auto v_item = [](int jj) { return 2 * jj + 2; };
+  auto issue_item = [&](int i) {  // a loader thread; nothing past the CTA's key tiles
+    const int jj = item_tile(i);
+    if (jj >= nk) return;
+    const bool is_k = i == 0 || (i & 1);
+    prefill_load_kv<D>(is_k ? &p.kmap : &p.vmap, sm + (i % S::SLOTS) * S::TILE, &bar[BAR_R0 + i % S::SLOTS], pids, jp0,
+                       j_begin + jj, lg_p);
+    last_item[i % S::SLOTS] = i;
+  };
+  auto wait_item = [&](int i) { return mbar_wait(&bar[BAR_R0 + i % S::SLOTS], (i / S::SLOTS) & 1, p.wait_limit); };
+  griddep_wait();  // the chunk's own rows, appended by a preceding dependent-launch append, are visible from here
+  if (tid == 0)
+    for (int i = 0; i < S::SLOTS; ++i) issue_item(i);
   // Q row -> TMEM columns [T::Q, T::Q + D/2), two bf16 per column
 #pragma unroll
   for (int c16 = 0; c16 < D / 32; ++c16) tc::tmem_st16(tb + lane_base + T::Q + c16 * 16, *reinterpret_cast<uint32_t(*)[16]>(&w[16 * c16]));
@@ -241,175 +267,207 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
 
   constexpr uint32_t id_qk = tc::idesc_bf16_f32(kTileM, kTileN, false);
   constexpr uint32_t id_pv = tc::idesc_bf16_f32(kTileM, D, true);
-  // S(j) = Q K(j)^T into the S columns from key buffer j % 2 (thread 0; K(j) has landed)
-  auto issue_qk = [&](int j) {
-    const unsigned char* K = Ks + (j & 1) * S::TILE;
+  // S(jj) = Q K(jj)^T into S buffer jj % 2 (thread 0; K(jj) has landed)
+  auto issue_qk = [&](int jj) {
+    const unsigned char* K = sm + (k_item(jj) % S::SLOTS) * S::TILE;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const unsigned char* kb = K + (kk / 4) * S::KH + (kk % 4) * 32;
-      tc::mma_bf16_ts(tb + T::S, tb + T::Q + kk * 8, tc::smem_desc(kb, 16, 1024), id_qk, kk > 0);
+      tc::mma_bf16_ts(tb + T::S + (jj & 1) * kTileN, tb + T::Q + kk * 8, tc::smem_desc(kb, 16, 1024), id_qk, kk > 0);
     }
-    tc::mma_commit(&bar[BAR_S]);
+    tc::mma_commit(&bar[BAR_S0 + (jj & 1)]);
+    log.issue(BAR_S0 + (jj & 1));
   };
-  // O += P(j) V(j), P as (hi, lo) from the S columns
-  auto issue_pv = [&](int j) {
+  // O += P(jj) V(jj), P as (hi, lo) from S buffer jj % 2
+  auto issue_pv = [&](int jj) {
+    const unsigned char* Vt = sm + (v_item(jj) % S::SLOTS) * S::TILE;
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
-      const uint64_t vb = tc::smem_desc(Vs + kk * 2048, S::KH, 1024);  // 16 keys of the MN-major value tile
-      const uint32_t ph = tb + T::S + (kk / 2) * 32 + (kk % 2) * 8;   // hi of keys 16kk .. 16kk+15; lo 16 columns on
-      tc::mma_bf16_ts(tb + T::O, ph, vb, id_pv, j > 0 || kk > 0);
+      const uint64_t vb = tc::smem_desc(Vt + kk * 2048, S::KH, 1024);  // 16 keys of the MN-major value tile
+      const uint32_t ph = tb + T::S + (jj & 1) * kTileN + (kk / 2) * 32 + (kk % 2) * 8;  // hi of keys 16kk .. +15; lo 16 columns on
+      tc::mma_bf16_ts(tb + T::O, ph, vb, id_pv, jj > 0 || kk > 0);
       tc::mma_bf16_ts(tb + T::O, ph + 16, vb, id_pv, true);
     }
     tc::mma_commit(&bar[BAR_O]);
+    log.issue(BAR_O);
   };
 
-  // Key tile j: P.V(j-1) done (it has left the S columns and the value buffer)
-  // -> V(j) into the value buffer, S(j) -> softmax -> P.V(j).  Every barrier has
-  // at most one phase outstanding; every wait is bounded.
+  // Key tile j: S(j) done -> softmax(j) -> P.V(j).  Three threads issue the
+  // asynchronous work, each also a softmax row: thread 0 the copies, thread 32
+  // S(j+1) during softmax(j) (once P.V(j-1) has left the other S buffer and
+  // K(j+1) has landed), thread 64 P.V(j).  A tensor-core MMA of these shapes
+  // keeps its issuing thread about 100 cycles, so spreading the MMAs over two
+  // warps keeps either from holding back the block by a whole key tile.  The
+  // threads meet once per key tile, before P.V(j).  Every barrier has at most
+  // one phase outstanding; every wait is bounded.
+  constexpr int kLoader = 0, kSIssuer = 32, kPvIssuer = 64, kVLoader = 96;
   float m_ref = -INFINITY, l_run = 0.0f;
   bool ok = !(p.debug_stall && nk > 0) || mbar_wait(&bar[BAR_STALL], 0, p.wait_limit);  // the stall runs out
-  // thread 0's own waits; a failure there reaches the others through the next
-  // collective wait (theirs then runs out too: bounded)
-  bool issuer_ok = true;
-  const uint32_t col_s = tb + lane_base + T::S;
+  // a role thread's own waits; a failure there reaches the others at the next
+  // block-wide meeting (their waits on its work run out too: bounded)
+  bool role_ok = true;
+  if (tid == kSIssuer && nk > 0 && ok) {
+    role_ok = wait_item(k_item(0));
+    if (role_ok) {
+      tc::fence_after_sync();
+      issue_qk(0);
+    }
+  }
+  bool next_k_slot_refilled = false;  // thread 96: S(j)'s key slot already took its next item
   for (int j = 0; j < nk && ok; ++j) {
-    if (tid == 0 && issuer_ok) {
-      if (j > 0) {
-        issuer_ok = mbar_wait(&bar[BAR_O], (j - 1) & 1, p.wait_limit);
-        if (issuer_ok) {
-          log.seen(BAR_O);
-          prefill_load_kv<D>(p, &p.vmap, Vs, &bar[BAR_V], pids, jp0, j_begin + j, h, fallback_pid);
-          log.issue(BAR_V);
-        }
-      }
-      if (issuer_ok) issuer_ok = mbar_wait(&bar[BAR_K0 + (j & 1)], (j >> 1) & 1, p.wait_limit);
-      if (issuer_ok) {
-        log.seen(BAR_K0 + (j & 1));
-        tc::fence_after_sync();
-        issue_qk(j);
-        log.issue(BAR_S);
-      }
-    }
-    // ---- S(j) done
-    if (!(ok = __syncthreads_and(issuer_ok && mbar_wait(&bar[BAR_S], j & 1, p.wait_limit)))) break;
+    // ---- S(j) done (each warp waits for itself)
+    bool good = __all_sync(0xffffffffu, mbar_wait(&bar[BAR_S0 + (j & 1)], (j >> 1) & 1, p.wait_limit));
     tc::fence_after_sync();
-    if (tid == 0) {
-      log.seen(BAR_S);
-      if (j + 2 < nk) {  // S(j) has read key buffer j % 2: refill it
-        prefill_load_kv<D>(p, &p.kmap, Ks + (j & 1) * S::TILE, &bar[BAR_K0 + (j & 1)], pids, jp0, j_begin + j + 2, h,
-                           fallback_pid);
-        log.issue(BAR_K0 + (j & 1));
-      }
+    // S(j) has read K(j): its slot takes the item three on, K(2) after S(0)
+    // (thread 0 issues key tiles), V(j) after S(j > 0) (thread 96 value tiles)
+    if (good && tid == (j == 0 ? kLoader : kVLoader)) {
+      if (!next_k_slot_refilled) issue_item(k_item(j) + S::SLOTS);
+      next_k_slot_refilled = false;
     }
+    if (good && tid == kSIssuer) log.seen(BAR_S0 + (j & 1));
+    const uint32_t col_s = tb + lane_base + T::S + (j & 1) * kTileN;
+    const int key0 = (j_begin + j) * kTileN;
+    float alpha = 1.0f;
     // ---- online softmax of this row's 64 scores (log2 domain), in two halves of
     // 32 read from tensor memory twice (for the maximum, then for the weights),
     // so that no more than 32 scores are live in registers
-    const int key0 = (j_begin + j) * kTileN;
     const bool edge = key0 + kTileN - 1 > my_pos;  // the row's causal edge (or keys past the chunk) is in this tile
-    float mx = -INFINITY;
+    if (good) {
+      float mx = -INFINITY;
 #pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      float sc[32];
-      tc::tmem_ld32(col_s + 32 * half, sc);
-      if (edge) {
+      for (int half = 0; half < 2; ++half) {
+        float sc[32];
+        tc::tmem_ld32(col_s + 32 * half, sc);
+        if (edge) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (key0 + 32 * half + i > my_pos) sc[i] = -INFINITY;
-      }
-      float mx4[4] = {sc[0], sc[1], sc[2], sc[3]};
-#pragma unroll
-      for (int i = 4; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], sc[i]);
-      mx = fmaxf(mx, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])));
-    }
-    mx = __fmul_rn(mx, p.sm_scale_log2);  // the scale is positive: the largest scaled score is the scaled largest one
-    float alpha = 1.0f;
-    if (mx > __fadd_rn(m_ref, kRescaleSlack)) {
-      alpha = ex2(__fsub_rn(m_ref, mx));
-      m_ref = mx;
-      l_run = __fmul_rn(l_run, alpha);
-    }
-    // every score so far masked: the weights are ex2(-inf) = 0 against any finite reference
-    const float neg_ref = m_ref == -INFINITY ? 0.0f : -m_ref;
-    // weights -> (hi, lo) bf16 pairs in place of S: keys 32h .. 32h+31 as hi
-    // in columns 32h .. 32h+15 and lo in the 16 after them
-    float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      float sc[32];
-      tc::tmem_ld32(col_s + 32 * half, sc);
-      if (edge) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (key0 + 32 * half + i > my_pos) sc[i] = -INFINITY;
-      }
-#pragma unroll
-      for (int q8 = 0; q8 < 2; ++q8) {
-        uint32_t hw[8], lw[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float a = ex2(fmaf(sc[16 * q8 + 2 * i], p.sm_scale_log2, neg_ref));
-          const float c = ex2(fmaf(sc[16 * q8 + 2 * i + 1], p.sm_scale_log2, neg_ref));
-          ls[i] = __fadd_rn(ls[i], __fadd_rn(a, c));
-          const __nv_bfloat162 hi = __floats2bfloat162_rn(a, c);
-          const __nv_bfloat162 lo = __floats2bfloat162_rn(__fsub_rn(a, __low2float(hi)), __fsub_rn(c, __high2float(hi)));
-          hw[i] = *reinterpret_cast<const uint32_t*>(&hi);
-          lw[i] = *reinterpret_cast<const uint32_t*>(&lo);
+          for (int i = 0; i < 32; ++i)
+            if (key0 + 32 * half + i > my_pos) sc[i] = -INFINITY;
         }
-        tc::tmem_st8(col_s + 32 * half + q8 * 8, hw);
-        tc::tmem_st8(col_s + 32 * half + 16 + q8 * 8, lw);
+        float mx4[4] = {sc[0], sc[1], sc[2], sc[3]};
+#pragma unroll
+        for (int i = 4; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], sc[i]);
+        mx = fmaxf(mx, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])));
+      }
+      mx = __fmul_rn(mx, p.sm_scale_log2);  // the scale is positive: the largest scaled score is the scaled largest one
+      if (mx > __fadd_rn(m_ref, kRescaleSlack)) {
+        alpha = ex2(__fsub_rn(m_ref, mx));
+        m_ref = mx;
+        l_run = __fmul_rn(l_run, alpha);
       }
     }
-    const float lsum = __fadd_rn(__fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3])),
-                                 __fadd_rn(__fadd_rn(ls[4], ls[5]), __fadd_rn(ls[6], ls[7])));
-    l_run = __fadd_rn(l_run, lsum);
-    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-      // the reference max moved: rescale O (P.V(j-1), its last writer, is done:
-      // thread 0 saw it before issuing S(j); the others see it here)
-      if (mbar_wait(&bar[BAR_O], (j - 1) & 1, p.wait_limit)) {
+    // ---- P.V(j-1) done: thread 0 refills its value slot (with K(j+2)); thread
+    // 32 then issues S(j+1) into the other S buffer once K(j+1) has landed
+    if (good && role_ok && j > 0 && (tid == kLoader || tid == kSIssuer)) {
+      role_ok = mbar_wait(&bar[BAR_O], (j - 1) & 1, p.wait_limit);
+      if (role_ok && tid == kLoader) issue_item(v_item(j - 1) + S::SLOTS);
+    }
+    if (good && role_ok && tid == kSIssuer && j + 1 < nk) {
+      role_ok = wait_item(k_item(j + 1));
+      if (role_ok) {
         tc::fence_after_sync();
+        issue_qk(j + 1);
+      }
+    }
+    if (good) {
+      // every score so far masked: the weights are ex2(-inf) = 0 against any finite reference
+      const float neg_ref = m_ref == -INFINITY ? 0.0f : -m_ref;
+      // weights -> (hi, lo) bf16 pairs in place of S: keys 32h .. 32h+31 as hi
+      // in columns 32h .. 32h+15 and lo in the 16 after them
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-        for (int c4 = 0; c4 < D / 32; ++c4) {
-          float o[32];
-          tc::tmem_ld32(tb + lane_base + T::O + c4 * 32, o);
+      for (int half = 0; half < 2; ++half) {
+        float sc[32];
+        tc::tmem_ld32(col_s + 32 * half, sc);
+        if (edge) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __fmul_rn(o[i], alpha);
-          tc::tmem_st32(tb + lane_base + T::O + c4 * 32, o);
+          for (int i = 0; i < 32; ++i)
+            if (key0 + 32 * half + i > my_pos) sc[i] = -INFINITY;
         }
-      } else {
-        ok = false;
+#pragma unroll
+        for (int q8 = 0; q8 < 2; ++q8) {
+          uint32_t hw[8], lw[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float a = ex2(fmaf(sc[16 * q8 + 2 * i], p.sm_scale_log2, neg_ref));
+            const float c = ex2(fmaf(sc[16 * q8 + 2 * i + 1], p.sm_scale_log2, neg_ref));
+            ls[i] = __fadd_rn(ls[i], __fadd_rn(a, c));
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(a, c);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(__fsub_rn(a, __low2float(hi)), __fsub_rn(c, __high2float(hi)));
+            hw[i] = *reinterpret_cast<const uint32_t*>(&hi);
+            lw[i] = *reinterpret_cast<const uint32_t*>(&lo);
+          }
+          tc::tmem_st8(col_s + 32 * half + q8 * 8, hw);
+          tc::tmem_st8(col_s + 32 * half + 16 + q8 * 8, lw);
+        }
+      }
+      const float lsum = __fadd_rn(__fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3])),
+                                   __fadd_rn(__fadd_rn(ls[4], ls[5]), __fadd_rn(ls[6], ls[7])));
+      l_run = __fadd_rn(l_run, lsum);
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        // the reference max moved: rescale O (P.V(j-1), its last writer, is done:
+        // threads 0 and 32 saw it before S(j+1); the others see it here)
+        if (__all_sync(0xffffffffu, mbar_wait(&bar[BAR_O], (j - 1) & 1, p.wait_limit))) {
+          tc::fence_after_sync();
+#pragma unroll 1
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            float o[32];
+            tc::tmem_ld32(tb + lane_base + T::O + c4 * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __fmul_rn(o[i], alpha);
+            tc::tmem_st32(tb + lane_base + T::O + c4 * 32, o);
+          }
+        } else {
+          good = false;
+        }
       }
     }
     tc::tmem_wait_st();
     // ---- value tile: keys past the chunk's last position may hold stale or
     // poisoned values; zero those rows so that 0-weights never meet a NaN
-    if (!(ok = __syncthreads_and(ok && issuer_ok && mbar_wait(&bar[BAR_V], j & 1, p.wait_limit)))) break;
+    const int vi = v_item(j);
+    if (!(ok = __syncthreads_and(good && role_ok && wait_item(vi)))) break;
     if (key0 + kTileN - 1 > p_last) {
+      unsigned char* Vt = sm + (vi % S::SLOTS) * S::TILE;
       const int first = max(0, p_last + 1 - key0);
       const int n16 = (kTileN - first) * NH * 8;  // 16-byte pieces to clear
       for (int i = tid; i < n16; i += kTileM) {
         const int row = first + i / (NH * 8), piece = i % (NH * 8);
-        *reinterpret_cast<uint4*>(Vs + (piece / 8) * S::KH + row * 128 + (piece % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(Vt + (piece / 8) * S::KH + row * 128 + (piece % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
       tc::fence_proxy_async_smem();
     }
     tc::fence_before_sync();
     __syncthreads();
     // ---- O += P V
-    if (tid == 0) {
-      log.seen(BAR_V);
+    if (tid == kPvIssuer) {
       tc::fence_after_sync();
       issue_pv(j);
-      log.issue(BAR_O);
+    }
+    if (tid == kVLoader) {
+      // S(j+1) has usually finished by now: its key slot takes its next item
+      // (V(j+1)) a little earlier
+      if (j + 1 < nk && mbar_test(&bar[BAR_S0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1)) {
+        issue_item(k_item(j + 1) + S::SLOTS);
+        next_k_slot_refilled = true;
+      }
     }
   }
   if (ok && nk > 0) {
     // the last commit arrives when every MMA before it has completed too
     ok = __syncthreads_and(mbar_wait(&bar[BAR_O], (nk - 1) & 1, p.wait_limit));
-    if (ok && tid == 0) log.seen(BAR_O);
+    if (ok && tid == kPvIssuer) log.seen(BAR_O);
   }
-  if (!ok && tid == 0) {
-    record_error(p.status, ST_TIMEOUT);
-    log.drain(bar);  // every copy and MMA in flight finishes before TMEM or shared memory is reused
+  if (!ok) {
+    // every copy and MMA in flight finishes before TMEM or shared memory is
+    // reused: each MMA issuer drains its barriers; thread 0 the ring slots,
+    // whose loads two threads issue (each slot's last one, at most one in flight)
+    __syncthreads();
+    if (tid == kSIssuer || tid == kPvIssuer) log.drain(bar);
+    if (tid == kLoader) {
+      record_error(p.status, ST_TIMEOUT);
+      for (int r = 0; r < S::SLOTS; ++r)
+        if (last_item[r] >= 0) mbar_wait(&bar[BAR_R0 + r], (last_item[r] / S::SLOTS) & 1, kDrainWaitLimit);
+    }
   }
   __syncthreads();
   if (nk > 0) {
@@ -440,10 +498,16 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
     } else {
       // publish this key range's partial (max, sum, unnormalised O) -- an empty
       // one after a failure, so that the counters still return to zero -- and
-      // let the last of the tile's CTAs merge the ranges in ascending order
-      const size_t slot0 = (static_cast<size_t>(p.chunk_row_begin[c] + t0 + min(r_local, rows_here - 1)) * p.Hq +
-                            h * G + g) * p.tile_splits;
-      const size_t slot = slot0 + split;
+      // let the last of the tile's CTAs merge the ranges in ascending order.
+      // A tile's partials are tile-major: per key range, D / CB blocks of CB
+      // columns, each [CB / 4][128 rows][4] floats (one key or value buffer's
+      // size), so that a warp's 16-byte stores and the merge's bulk copies
+      // are contiguous; the (max, sum) pairs are [key range][128 rows].
+      constexpr int CB = S::TILE / (kTileM * 4);  // columns per block
+      constexpr int NBS = D / CB;                 // blocks per key range
+      const int ti = p.chunk_tile_begin[c] + mt * p.Hkv + h;  // the tile (its counter)
+      const size_t blk0 = static_cast<size_t>(ti) * p.tile_splits;
+      float* po = p.ws_tile_o + (blk0 + split) * (kTileM * D);
 #pragma unroll 1
       for (int c4 = 0; c4 < D / 32; ++c4) {
         float o[32];
@@ -453,108 +517,100 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0.0f;
         }
-        if (row_valid) {
-          float4* dst = reinterpret_cast<float4*>(p.ws_tile_o + slot * D + c4 * 32);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        for (int i = 0; i < 8; ++i) {
+          const int col = c4 * 32 + 4 * i;
+          float4* dst = reinterpret_cast<float4*>(po + (col / CB) * (kTileM * CB)) + ((col % CB) / 4) * kTileM + m;
+          *dst = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         }
       }
-      if (row_valid) {
-        p.ws_tile_ml[slot * 2] = ok ? m_ref : -INFINITY;
-        p.ws_tile_ml[slot * 2 + 1] = ok ? l_run : 0.0f;
-      }
+      reinterpret_cast<float2*>(p.ws_tile_ml)[(blk0 + split) * kTileM + m] =
+          make_float2(ok ? m_ref : -INFINITY, ok ? l_run : 0.0f);
       __threadfence();
       __syncthreads();
-      int32_t* counter = p.ws_tile_count + p.chunk_tile_begin[c] + mt * p.Hkv + h;
+      int32_t* counter = p.ws_tile_count + ti;
       if (tid == 0) *last_flag = atomicAdd(counter, 1) == nsplit - 1;
       __syncthreads();
       if (*last_flag) {
         __threadfence();
-        // Merge in ascending key-range order.  Each row's weights f[row][sp] and
-        // 1 / sum go to shared memory (the K/V buffers are free now); then all
-        // threads sweep the tile in 16-byte pieces (thread t: pieces t, t + 128,
-        // ...; a row's pieces are consecutive), eight loads in flight a thread
-        // (four pieces, two key ranges): the merge is bound by the loads one SM
-        // keeps in flight.
-        float* ftab = reinterpret_cast<float*>(sm);  // [kTileM][nsplit], then [kTileM] inverse sums
-        const bool fits = (kTileM * (nsplit + 1)) * 4 <= S::BAR_OFF;
-        if (fits) {
-          float M = -INFINITY;
+        // Merge in ascending key-range order.  Row m's max and 1 / sum first;
+        // then the partial blocks stream through the three key and value
+        // buffers (free now) by bulk copies, several in flight, in the order
+        // (column block, key range); each thread accumulates its row's CB
+        // columns of a block.
+        const float2* mlt = reinterpret_cast<const float2*>(p.ws_tile_ml) + blk0 * kTileM;
+        const float* pbase = p.ws_tile_o + blk0 * (kTileM * D);
+        const int nb = NBS * nsplit;
+        auto issue_block = [&](int b) {  // block b: column block b / nsplit of key range b % nsplit
+          uint64_t* mb = &bar[BAR_M0 + b % kMergeSlots];
+          mbar_arrive_expect_tx(mb, static_cast<uint32_t>(S::TILE));
+          bulk_g2s(sm + (b % kMergeSlots) * S::TILE,
+                   pbase + static_cast<size_t>(b % nsplit) * (kTileM * D) + (b / nsplit) * (kTileM * CB),
+                   static_cast<uint32_t>(S::TILE), mb, l2_policy_evict_first());
+        };
+        int issued = 0;
+        if (tid == 0) {
+          fence_proxy_async_global();  // the other CTAs' partials, seen through the counter, before the bulk reads
+          for (; issued < min(kMergeSlots, nb); ++issued) issue_block(issued);
+        }
+        float M = -INFINITY;
 #pragma unroll 4
-          for (int sp = 0; sp < nsplit; ++sp) {  // independent loads, several in flight
-            const float mv = row_valid ? __ldcg(p.ws_tile_ml + (slot0 + sp) * 2) : 0.0f;
-            ftab[m * nsplit + sp] = mv;
-            M = fmaxf(M, mv);
-          }
-          float lsum = 0.0f;
+        for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(mlt + sp * kTileM + m).x);
+        float lsum = 0.0f;
 #pragma unroll 4
-          for (int sp = 0; sp < nsplit; ++sp) {
-            const float f = ex2(__fsub_rn(ftab[m * nsplit + sp], M));
-            ftab[m * nsplit + sp] = f;
-            lsum = fmaf(f, row_valid ? __ldcg(p.ws_tile_ml + (slot0 + sp) * 2 + 1) : 1.0f, lsum);
-          }
-          ftab[kTileM * nsplit + m] = __fdiv_rn(1.0f, lsum);
-          __syncthreads();
-          constexpr int PPR = D / 4;  // 16-byte pieces per row
-          constexpr int U = 4;        // pieces per thread per sweep step
+        for (int sp = 0; sp < nsplit; ++sp) {
+          const float2 v = __ldcg(mlt + sp * kTileM + m);
+          lsum = fmaf(ex2(__fsub_rn(v.x, M)), v.y, lsum);
+        }
+        const float inv = __fdiv_rn(1.0f, lsum);
+        bool mok = true;
 #pragma unroll 1
-          for (int q0 = tid; q0 < kTileM * PPR; q0 += kTileM * U) {
-            float4 acc[U];
-            const float4* src[U];
-            int rr[U];
-            bool use[U];
+        for (int cb = 0; cb < NBS && mok; ++cb) {
+          float acc[CB];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-              const int q = q0 + u * kTileM;
-              rr[u] = q / PPR;
-              const int rl = rr[u] / G, gg = rr[u] % G;
-              use[u] = q < kTileM * PPR && rr[u] < R * G && rl < rows_here;
-              const size_t s0 = (static_cast<size_t>(p.chunk_row_begin[c] + t0 + (use[u] ? rl : 0)) * p.Hq + h * G + gg) *
-                                p.tile_splits;
-              src[u] = reinterpret_cast<const float4*>(p.ws_tile_o + s0 * D) + q % PPR;
-              acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll 2
-            for (int sp = 0; sp < nsplit; ++sp) {
+          for (int i = 0; i < CB; ++i) acc[i] = 0.0f;
+#pragma unroll 1
+          for (int sp = 0; sp < nsplit; ++sp) {
+            const int b = cb * nsplit + sp;
+            const float mv = __ldcg(mlt + sp * kTileM + m).x;
+            const bool got = mbar_wait(&bar[BAR_M0 + b % kMergeSlots], (b / kMergeSlots) & 1, p.wait_limit);
+            if (got) {
+              const float f = ex2(__fsub_rn(mv, M));
+              const float4* src = reinterpret_cast<const float4*>(sm + (b % kMergeSlots) * S::TILE) + m;
 #pragma unroll
-              for (int u = 0; u < U; ++u) {
-                if (!use[u]) continue;
-                const float f = ftab[rr[u] * nsplit + sp];
-                const float4 v = __ldcg(src[u] + static_cast<size_t>(sp) * PPR);
-                acc[u].x = fmaf(f, v.x, acc[u].x);
-                acc[u].y = fmaf(f, v.y, acc[u].y);
-                acc[u].z = fmaf(f, v.z, acc[u].z);
-                acc[u].w = fmaf(f, v.w, acc[u].w);
+              for (int i = 0; i < CB / 4; ++i) {
+                const float4 v = src[i * kTileM];
+                acc[4 * i] = fmaf(f, v.x, acc[4 * i]);
+                acc[4 * i + 1] = fmaf(f, v.y, acc[4 * i + 1]);
+                acc[4 * i + 2] = fmaf(f, v.z, acc[4 * i + 2]);
+                acc[4 * i + 3] = fmaf(f, v.w, acc[4 * i + 3]);
               }
             }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-              if (!use[u]) continue;
-              const int q = q0 + u * kTileM, rl = rr[u] / G, gg = rr[u] % G;
-              const float inv = ftab[kTileM * nsplit + rr[u]];
-              const __nv_bfloat162 lo = __floats2bfloat162_rn(__fmul_rn(acc[u].x, inv), __fmul_rn(acc[u].y, inv));
-              const __nv_bfloat162 hi = __floats2bfloat162_rn(__fmul_rn(acc[u].z, inv), __fmul_rn(acc[u].w, inv));
-              __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(rb + t0 + rl) * p.Hq + h * G + gg) * D;
-              *reinterpret_cast<uint2*>(orow + (q % PPR) * 4) =
-                  make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+            if (!(mok = __syncthreads_and(got))) break;  // every thread is done with the slot
+            if (tid == 0 && issued < nb) {
+              tc::fence_proxy_async_smem();
+              issue_block(issued++);
             }
           }
-        } else if (row_valid) {
-          float M = -INFINITY;
-          for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(p.ws_tile_ml + (slot0 + sp) * 2));
-          float lsum = 0.0f;
-          for (int sp = 0; sp < nsplit; ++sp)
-            lsum = fmaf(ex2(__fsub_rn(__ldcg(p.ws_tile_ml + (slot0 + sp) * 2), M)),
-                        __ldcg(p.ws_tile_ml + (slot0 + sp) * 2 + 1), lsum);
-          const float inv = __fdiv_rn(1.0f, lsum);
-          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + row_off;
-          for (int d = 0; d < D; ++d) {
-            float acc = 0.0f;
-            for (int sp = 0; sp < nsplit; ++sp)
-              acc = fmaf(ex2(__fsub_rn(__ldcg(p.ws_tile_ml + (slot0 + sp) * 2), M)),
-                         __ldcg(p.ws_tile_o + (slot0 + sp) * D + d), acc);
-            orow[d] = __float2bfloat16_rn(__fmul_rn(acc, inv));
+          if (mok && row_valid) {
+            __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + row_off + cb * CB;
+#pragma unroll
+            for (int i = 0; i < CB / 8; ++i) {
+              uint32_t w[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(__fmul_rn(acc[8 * i + 2 * k], inv),
+                                                                __fmul_rn(acc[8 * i + 2 * k + 1], inv));
+                w[k] = *reinterpret_cast<const uint32_t*>(&pr);
+              }
+              *reinterpret_cast<uint4*>(orow + 8 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
           }
+        }
+        if (!mok && tid == 0) {
+          record_error(p.status, ST_TIMEOUT);
+          for (int b = max(0, issued - kMergeSlots); b < issued; ++b)  // copies in flight land before the CTA leaves
+            mbar_wait(&bar[BAR_M0 + b % kMergeSlots], (b / kMergeSlots) & 1, kDrainWaitLimit);
         }
         if (tid == 0) *counter = 0;  // leave the workspace zero-filled for the next call
       }

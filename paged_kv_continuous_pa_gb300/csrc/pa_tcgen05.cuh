@@ -160,6 +160,12 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 
 // ---------------------------------------------------------- tensor-map TMA --
 
+// Bring a tensor map (a kernel parameter) into the copy engine's descriptor
+// cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // 2-D tiled load of the box at element coordinates (x, y) into shared memory,
 // completion counted in bytes on `bar`.  x * element size must be a multiple
 // of 16 bytes.
