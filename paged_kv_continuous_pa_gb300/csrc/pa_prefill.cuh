@@ -105,20 +105,21 @@ struct PrefillIssueLog {
 // keys x 64 head elements per page piece and head-dim half.  ybase[jp - jp0]
 // is the tensor-map row of page jp's first slot for this kv head (built once
 // from the block table; a page past the sequence has a valid page's row:
-// masked or zeroed later).  P = 2^lg_p.  The issuing thread reads shared
-// memory only: no kernel parameter, no division.
+// masked or zeroed later).  P = 2^lg_p.  Called by all lanes of one warp:
+// lane 0 posts the byte count, then lane l issues box l (2 to 8 boxes), so a
+// tile's copies cost the warp about one copy's issue time.
 template <int D>
 __device__ __forceinline__ void prefill_load_kv(const CUtensorMap* map, unsigned char* dst, uint64_t* bar,
-                                                const int32_t* ybase, int jp0, int j, int lg_p) {
+                                                const int32_t* ybase, int jp0, int j, int lg_p, int lane) {
   constexpr int NH = D / 64;
   const int lg_br = lg_p < 6 ? lg_p : 6;  // rows of one box: a page, or a 64-key part of a larger page
-  mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kTileN * D * 2));
-  for (int k = 0; k < (kTileN >> lg_br); ++k) {
+  if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kTileN * D * 2));
+  __syncwarp();
+  if (lane < (kTileN >> lg_br) * NH) {
+    const int k = lane / NH, half = lane % NH;
     const int t = j * kTileN + (k << lg_br);  // first key of the box
     const int y = ybase[(t >> lg_p) - jp0] + (t & ((1 << lg_p) - 1));
-#pragma unroll
-    for (int half = 0; half < NH; ++half)
-      tc::tma_load_2d(dst + half * PrefillSmem<D>::KH + (k << lg_br) * 128, map, half * 64, y, bar);
+    tc::tma_load_2d(dst + half * PrefillSmem<D>::KH + (k << lg_br) * 128, map, half * 64, y, bar);
   }
 }
 
@@ -245,17 +246,18 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
   auto item_tile = [](int i) { return i == 0 ? 0 : ((i & 1) ? (i + 1) / 2 : (i - 2) / 2); };
   auto k_item = [](int jj) { return jj == 0 ? 0 : 2 * jj - 1; };
   auto v_item = [](int jj) { return 2 * jj + 2; };
-  auto issue_item = [&](int i) {  // a loader thread; nothing past the CTA's key tiles
+  const int lane = tid & 31;
+  auto issue_item = [&](int i) {  // all lanes of a loader warp; nothing past the CTA's key tiles
     const int jj = item_tile(i);
     if (jj >= nk) return;
     const bool is_k = i == 0 || (i & 1);
     prefill_load_kv<D>(is_k ? &p.kmap : &p.vmap, sm + (i % S::SLOTS) * S::TILE, &bar[BAR_R0 + i % S::SLOTS], pids, jp0,
-                       j_begin + jj, lg_p);
-    last_item[i % S::SLOTS] = i;
+                       j_begin + jj, lg_p, lane);
+    if (lane == 0) last_item[i % S::SLOTS] = i;
   };
   auto wait_item = [&](int i) { return mbar_wait(&bar[BAR_R0 + i % S::SLOTS], (i / S::SLOTS) & 1, p.wait_limit); };
   griddep_wait();  // the chunk's own rows, appended by a preceding dependent-launch append, are visible from here
-  if (tid == 0)
+  if (warp == 0)
     for (int i = 0; i < S::SLOTS; ++i) issue_item(i);
   // Q row -> TMEM columns [T::Q, T::Q + D/2), two bf16 per column
 #pragma unroll
@@ -300,7 +302,8 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
   // warps keeps either from holding back the block by a whole key tile.  The
   // threads meet once per key tile, before P.V(j).  Every barrier has at most
   // one phase outstanding; every wait is bounded.
-  constexpr int kLoader = 0, kSIssuer = 32, kPvIssuer = 64, kVLoader = 96;
+  constexpr int kLoader = 0, kSIssuer = 32, kPvIssuer = 64;  // threads
+  constexpr int kKWarp = 0, kVWarp = 3;                       // warps that issue key / value tile copies
   float m_ref = -INFINITY, l_run = 0.0f;
   bool ok = !(p.debug_stall && nk > 0) || mbar_wait(&bar[BAR_STALL], 0, p.wait_limit);  // the stall runs out
   // a role thread's own waits; a failure there reaches the others at the next
@@ -313,14 +316,14 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
       issue_qk(0);
     }
   }
-  bool next_k_slot_refilled = false;  // thread 96: S(j)'s key slot already took its next item
+  bool next_k_slot_refilled = false;  // warp 3: S(j)'s key slot already took its next item
   for (int j = 0; j < nk && ok; ++j) {
     // ---- S(j) done (each warp waits for itself)
     bool good = __all_sync(0xffffffffu, mbar_wait(&bar[BAR_S0 + (j & 1)], (j >> 1) & 1, p.wait_limit));
     tc::fence_after_sync();
     // S(j) has read K(j): its slot takes the item three on, K(2) after S(0)
-    // (thread 0 issues key tiles), V(j) after S(j > 0) (thread 96 value tiles)
-    if (good && tid == (j == 0 ? kLoader : kVLoader)) {
+    // (warp 0 issues key tiles), V(j) after S(j > 0) (warp 3 value tiles)
+    if (good && warp == (j == 0 ? kKWarp : kVWarp)) {
       if (!next_k_slot_refilled) issue_item(k_item(j) + S::SLOTS);
       next_k_slot_refilled = false;
     }
@@ -355,11 +358,14 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
         l_run = __fmul_rn(l_run, alpha);
       }
     }
-    // ---- P.V(j-1) done: thread 0 refills its value slot (with K(j+2)); thread
+    // ---- P.V(j-1) done: warp 0 refills its value slot (with K(j+2)); thread
     // 32 then issues S(j+1) into the other S buffer once K(j+1) has landed
-    if (good && role_ok && j > 0 && (tid == kLoader || tid == kSIssuer)) {
+    if (good && role_ok && j > 0 && (warp == kKWarp || tid == kSIssuer)) {
       role_ok = mbar_wait(&bar[BAR_O], (j - 1) & 1, p.wait_limit);
-      if (role_ok && tid == kLoader) issue_item(v_item(j - 1) + S::SLOTS);
+      if (warp == kKWarp) {
+        role_ok = __all_sync(0xffffffffu, role_ok);
+        if (role_ok) issue_item(v_item(j - 1) + S::SLOTS);
+      }
     }
     if (good && role_ok && tid == kSIssuer && j + 1 < nk) {
       role_ok = wait_item(k_item(j + 1));
@@ -425,6 +431,7 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
     // ---- value tile: keys past the chunk's last position may hold stale or
     // poisoned values; zero those rows so that 0-weights never meet a NaN
     const int vi = v_item(j);
+    tc::fence_before_sync();
     if (!(ok = __syncthreads_and(good && role_ok && wait_item(vi)))) break;
     if (key0 + kTileN - 1 > p_last) {
       unsigned char* Vt = sm + (vi % S::SLOTS) * S::TILE;
@@ -435,18 +442,17 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
         *reinterpret_cast<uint4*>(Vt + (piece / 8) * S::KH + row * 128 + (piece % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
       tc::fence_proxy_async_smem();
+      __syncthreads();
     }
-    tc::fence_before_sync();
-    __syncthreads();
     // ---- O += P V
     if (tid == kPvIssuer) {
       tc::fence_after_sync();
       issue_pv(j);
     }
-    if (tid == kVLoader) {
+    if (warp == kVWarp && j + 1 < nk) {
       // S(j+1) has usually finished by now: its key slot takes its next item
       // (V(j+1)) a little earlier
-      if (j + 1 < nk && mbar_test(&bar[BAR_S0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1)) {
+      if (__shfl_sync(0xffffffffu, mbar_test(&bar[BAR_S0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1) ? 1 : 0, 0)) {
         issue_item(k_item(j + 1) + S::SLOTS);
         next_k_slot_refilled = true;
       }
