@@ -441,6 +441,33 @@ def workload_entry(env, name: str, steps: int, warmup: int, seqs: int = 0):
     return entry
 
 
+def row_groups_entry(env, steps: int, warmup: int):
+    """The shared-prefix step with its rows listed prefix by prefix, timed with
+    one row per tensor-core CTA and with row groups (pa_set_row_groups: the
+    pages all rows of a group share are staged once per CTA).  Output bits are
+    the same in every form; only the times differ."""
+    torch, pa, W = env.torch, env.pa, env.W
+    wl = W.group_by_prefix(W.shared_prefix())
+    st = env.pa_setup.upload(wl, device=env.dev)
+    alg = wl.kv_bytes_unique() + wl.qo_bytes()
+    peak, _ = measured_peaks()
+    out = {"workload": wl.description, "rows": wl.n_rows, "times": {}}
+    old = pa.get_row_groups()
+    try:
+        for rg in (1, 2, 4, 8):
+            pa.set_row_groups(rg)
+            t = time_steps(env, st, wl, steps, warmup)
+            out["times"][str(rg)] = {"ms_per_step": t["ms_per_step"], "attention_ms": t["attention_ms"],
+                                     "frac": alg / (t["attention_ms"] / 1e3) / 1e9 / peak,
+                                     "clocks": t["clocks"]}
+    finally:
+        pa.set_row_groups(old)
+    del st
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -533,6 +560,7 @@ def run_ours(args):
         entries = {}
         for name in ALL_WORKLOADS:
             entries[name] = workload_entry(env, name, max(args.steps, 20), max(args.warmup, 3))
+        entries["shared_prefix_row_groups"] = row_groups_entry(env, max(args.steps, 20), max(args.warmup, 3))
 
     if rank == 0:
         line = {
