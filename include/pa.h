@@ -56,7 +56,7 @@ typedef enum {
     PA_ERR_UNSUPPORTED = 2, /* host-side: a valid but unimplemented shape (e.g. head_dim 96) */
     PA_ERR_OUT_OF_RANGE = 3, /* device-side: sequence id, position or page id out of range */
     PA_ERR_TIMEOUT = 4,     /* device-side: a bounded wait on a copy gave up */
-    PA_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, attribute, driver entry point) */
+    PA_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, attribute, driver entry point), or a kernel found its launch configuration inconsistent */
     PA_ERR_NO_PAGES = 6     /* host-side: an admission needs more free pages than the pool has */
 } pa_status;
 

@@ -458,7 +458,10 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
   }
   cudaError_t e = cudaErrorNotSupported;
   if (p.n_prefill_ctas > 0) {
-    e = pa::launch_mixed_bf16(p, s);
+    // every row on the tile path: a launch of tile CTAs of their own shape;
+    // else tiles and decode units share one launch (the tiles' bits are the
+    // same either way)
+    e = pl.total_rows == n_rows ? pa::launch_prefill_bf16(p, s) : pa::launch_mixed_bf16(p, s);
   } else if (mma_e4m3) {
     e = pa::launch_decode_e4m3_mma(p, s);
   } else if (mma_bf16) {

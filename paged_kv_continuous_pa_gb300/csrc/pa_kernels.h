@@ -43,7 +43,7 @@ constexpr int kDecodeRingBytes3 = 64 * 1024;                 // at three CTAs pe
 enum KvType { KV_F32 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
 
 // Device status codes (same values as pa_status in include/pa.h).
-enum { ST_OK = 0, ST_OUT_OF_RANGE = 3, ST_TIMEOUT = 4 };
+enum { ST_OK = 0, ST_OUT_OF_RANGE = 3, ST_TIMEOUT = 4, ST_LAUNCH = 5 };  // ST_LAUNCH: a kernel found its launch inconsistent
 
 constexpr int kMaxHeadScales = 64;  // kv heads a pool with per-head fp8 scales may have
 
@@ -239,6 +239,11 @@ cudaError_t launch_decode_bf16_mma(const AttnParams& p, cudaStream_t stream);
 // One launch whose first p.n_prefill_ctas CTAs run tensor-core prefill tiles
 // (bf16 q and K/V) and whose remaining CTAs run decode units.
 cudaError_t launch_mixed_bf16(const AttnParams& p, cudaStream_t stream);
+
+// A launch of tensor-core prefill tiles only (every row of the call is in a
+// chunk on the tile path): p.n_prefill_ctas warp-specialised tile CTAs with
+// the same per-row arithmetic as the tiles of launch_mixed_bf16.
+cudaError_t launch_prefill_bf16(const AttnParams& p, cudaStream_t stream);
 
 constexpr int kMinTileRows = 16;     // shorter chunks run on the decode path
 constexpr int kTileRowsTotal = 128;  // (position, head) rows of one tensor-core tile

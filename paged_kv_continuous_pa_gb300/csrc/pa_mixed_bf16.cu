@@ -20,7 +20,7 @@ __global__ void __launch_bounds__(DecodeGeom<D, G, KV_BF16>::THREADS, DecodeGeom
   static_assert(DecodeGeom<D, G, KV_BF16>::THREADS == kTileM, "a tile CTA has one thread per tile row");
   extern __shared__ __align__(128) unsigned char smem[];  // the tile and tensor-core units align to 1024 by hand
   if (static_cast<int>(blockIdx.x) < p.n_prefill_ctas) {
-    prefill_tile<D, G>(p, static_cast<int>(blockIdx.x), smem);
+    prefill_tile<D, G, false>(p, static_cast<int>(blockIdx.x), smem);
   } else {
     // a decode unit never allocates tensor memory: say so at once, or this CTA
     // would keep the SM's other CTA slots empty
@@ -38,7 +38,7 @@ cudaError_t launch_mixed_inst(const AttnParams& p0, cudaStream_t stream) {
   using Geo = DecodeGeom<D, G, KV_BF16>;
   AttnParams p = p0;
   p.n_stages = Geo::STAGES;
-  const size_t tile_smem = PrefillSmem<D>::BYTES;
+  const size_t tile_smem = PrefillLayout<D, false>::BYTES;
   const size_t dec_smem = (D == 128 && G >= 3) ? MmaBfGeom<G, 2>::SMEM
                                                : decode_smem_for<D, G, KV_BF16>(p.P, Geo::STAGES);
   const size_t smem = tile_smem > dec_smem ? tile_smem : dec_smem;

@@ -46,41 +46,62 @@ constexpr int kTileN = 64;   // keys per key tile
 
 constexpr int kTilePids = kTileSplitKeys / 16 + 1;  // page ids of one CTA's key range (pages >= 16 tokens)
 
-template <int D>
+template <int D, int SLOTS_>
 struct PrefillSmem {  // byte offsets from a 1024-byte aligned base
   static constexpr int NH = D / 64;        // 64-element halves of the head dim
   static constexpr int KH = kTileN * 128;  // one half of a K or V tile: 8 KiB
   static constexpr int TILE = NH * KH;     // one K or V tile
-  static constexpr int SLOTS = 3;          // ring of key / value tiles, from offset 0
-  static constexpr int BAR_OFF = SLOTS * TILE;  // barriers, then the TMEM slot (+112) and the last-CTA flag (+116)
-  static constexpr int PID_OFF = BAR_OFF + 128;
+  static constexpr int SLOTS = SLOTS_;     // key / value tile buffers, from offset 0
+  static constexpr int BAR_OFF = SLOTS * TILE;  // barriers and small state (256 bytes), then the page rows
+  static constexpr int TSLOT_OFF = BAR_OFF + 248;  // the TMEM base address
+  static constexpr int LAST_OFF = BAR_OFF + 252;   // this CTA merges the tile's key ranges
+  static constexpr int PID_OFF = BAR_OFF + 256;
   static constexpr int TOTAL = PID_OFF + ((kTilePids * 4 + 15) / 16) * 16;
   static constexpr int BYTES = TOTAL + 1024;  // slack for aligning the base
 };
 
+// The shared-memory layout of each tile CTA shape (its launcher sizes the
+// dynamic shared memory from the same definition)
+template <int D, bool WS>
+using PrefillLayout = PrefillSmem<D, WS ? 6 : 3>;
+
+// Barriers of the tile CTA that shares the decode CTA's shape (mixed launch)
 enum {
   BAR_R0 = 0,     // ring slot 0 / 1 / 2 landed (a key or a value tile)
   BAR_S0 = 3,     // S of S buffer 0 / 1 done
   BAR_O = 5,      // P.V of a key tile done
   BAR_STALL = 6,
   BAR_COUNT = 7,
-  BAR_M0 = 7,     // split merge: partial block landed in ring slot 0 / 1 / 2
+  BAR_M0 = 7,     // split merge: partial block landed in tile buffer 0 / 1 / 2
   BAR_ALL = 10    // barriers initialised (the merge's are not in the issue log)
+};
+// ... and of the warp-specialised tile CTA (a launch of chunk tiles only)
+enum {
+  WS_KF0 = 0,     // key buffer 0 / 1 / 2 landed
+  WS_VF0 = 3,     // value buffer 0 / 1 / 2 landed
+  WS_SD0 = 6,     // S of S buffer 0 / 1 / 2 done
+  WS_PR0 = 9,     // P of S buffer 0 / 1 / 2 written (one arrival per row)
+  WS_OD0 = 12,    // P.V of key tile j done, j % 3 = 0 / 1 / 2
+  WS_STALL = 15,
+  WS_COUNT = 16,
+  WS_M0 = 16,     // split merge, as above
+  WS_ALL = 19
 };
 constexpr int kMergeSlots = 3;
 
-// TMEM columns: two S buffers, S(j) in [64 (j % 2), 64 (j % 2) + 64), then
+// TMEM columns: SB S buffers, S(j) in buffer j % SB = [64 b, 64 b + 64), then
 // P(j) in place (keys 32h .. 32h+31: hi in columns 32h .. 32h+15, lo in the 16
-// after them); Q in [128, 128 + D/2); O in [256, 256 + D).  With two S
-// buffers S(j+1) runs on the tensor cores while the threads turn S(j) into
-// P(j), and P.V(j) while they start on S(j+1).
-template <int D>
+// after them); Q in [64 SB, 64 SB + D/2); O in [256, 256 + D).  With two S
+// buffers (the decode-shaped CTA) S(j+1) runs on the tensor cores while the
+// threads turn S(j) into P(j); the warp-specialised CTA keeps three, so that
+// S(j+1) waits only for P.V(j-2).
+template <int D, int SB>
 struct PrefillTmem {
   static constexpr uint32_t S = 0;  // S buffer b at S + 64 b
-  static constexpr uint32_t Q = 128;
+  static constexpr uint32_t Q = SB * kTileN;
   static constexpr uint32_t O = 256;
   static constexpr uint32_t COLS = 512;  // a power of two
-  static_assert(Q >= S + 2 * kTileN && O >= Q + D / 2 && O + D <= COLS, "tensor memory columns overlap");
+  static_assert(O >= Q + D / 2 && O + D <= COLS, "tensor memory columns overlap");
 };
 
 // A role thread's record of the copies and MMAs it issued on each barrier, in
@@ -95,8 +116,8 @@ struct PrefillIssueLog {
     pending |= 1u << b;
   }
   __device__ void seen(int b) { pending &= ~(1u << b); }
-  __device__ void drain(uint64_t* bar) {
-    for (int b = 0; b < BAR_COUNT; ++b)
+  __device__ void drain(uint64_t* bar, int count) {
+    for (int b = 0; b < count; ++b)
       if ((pending >> b) & 1u) mbar_wait(&bar[b], ((parity >> b) & 1u) ^ 1u, kDrainWaitLimit);
   }
 };
@@ -119,22 +140,42 @@ __device__ __forceinline__ void prefill_load_kv(const CUtensorMap* map, unsigned
     const int k = lane / NH, half = lane % NH;
     const int t = j * kTileN + (k << lg_br);  // first key of the box
     const int y = ybase[(t >> lg_p) - jp0] + (t & ((1 << lg_p) - 1));
-    tc::tma_load_2d(dst + half * PrefillSmem<D>::KH + (k << lg_br) * 128, map, half * 64, y, bar);
+    tc::tma_load_2d(dst + half * (kTileN * 128) + (k << lg_br) * 128, map, half * 64, y, bar);
   }
 }
 
-template <int D, int G>
+// One tile CTA.  WS = false: the decode CTA's shape (4 warps, 3 tile buffers),
+// in the launch that also runs decode units; WS = true: a launch of chunk
+// tiles only, 6 warps (4 softmax warps, one issuing the S MMAs and key-tile
+// copies, one the P.V MMAs and value-tile copies) and 6 tile buffers.  The
+// per-row arithmetic and its order are the same in both, so a chunk row's
+// output bits do not depend on which launch ran it.
+template <int D, int G, bool WS>
 __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsigned char* smem_raw) {
-  using S = PrefillSmem<D>;
-  using T = PrefillTmem<D>;
+  using S = PrefillLayout<D, WS>;
+  constexpr int NT = WS ? 192 : kTileM;  // threads of the CTA
+  constexpr int kBarAll = WS ? WS_ALL : BAR_ALL;
+  constexpr int kStall = WS ? WS_STALL : BAR_STALL;
+  constexpr int kM0 = WS ? WS_M0 : BAR_M0;
+  using T = PrefillTmem<D, WS ? 3 : 2>;
   constexpr int NH = S::NH;
+  {
+    // a launch that gave less shared memory than this layout needs touches none of it
+    uint32_t dyn;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (dyn < static_cast<uint32_t>(S::BYTES)) {
+      if (threadIdx.x == 0) record_error(p.status, ST_LAUNCH);
+      if (threadIdx.x < 32) tc::tmem_relinquish();
+      return;
+    }
+  }
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // ring slot r at sm + r * TILE
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S::BAR_OFF);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::BAR_OFF + 112);
-  int32_t* last_flag = reinterpret_cast<int32_t*>(sm + S::BAR_OFF + 116);
-  int32_t* last_item = reinterpret_cast<int32_t*>(sm + S::BAR_OFF + BAR_ALL * 8);  // per ring slot: last item issued
-  static_assert(BAR_ALL * 8 + S::SLOTS * 4 <= 112, "barriers overlap the TMEM slot");
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::TSLOT_OFF);
+  int32_t* last_flag = reinterpret_cast<int32_t*>(sm + S::LAST_OFF);
+  int32_t* last_item = reinterpret_cast<int32_t*>(sm + S::BAR_OFF + kBarAll * 8);  // per ring slot: last item issued
+  static_assert(kBarAll * 8 + S::SLOTS * 4 <= 248, "barriers overlap the TMEM slot");
   int32_t* pids = reinterpret_cast<int32_t*>(sm + S::PID_OFF);  // page ids, then tensor-map rows
 
   int c = 0;
@@ -182,7 +223,8 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
   // allocate tensor memory first: until it has, this CTA keeps others off the SM
   if (warp == 0) tc::tmem_alloc(tslot, T::COLS);
   if (tid == 0) {
-    for (int i = 0; i < BAR_ALL; ++i) mbar_init(&bar[i], 1);  // nothing ever arrives on BAR_STALL
+    for (int i = 0; i < kBarAll; ++i)  // nothing ever arrives on the stall barrier
+      mbar_init(&bar[i], (WS && i >= WS_PR0 && i < WS_PR0 + 3) ? kTileM : 1);
     for (int i = 0; i < S::SLOTS; ++i) last_item[i] = -1;
     fence_barrier_init();
     tc::prefetch_tensormap(&p.kmap);  // the copy issuer's descriptors, fetched while the setup runs
@@ -210,10 +252,10 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
   }
   bool bad = !geom_ok;
   if (geom_ok) {
-    for (int r = tid; r < rows_here; r += kTileM)
+    for (int r = tid; r < rows_here; r += NT)
       bad |= __ldg(p.seq_ids + rb + t0 + r) != seq || __ldg(p.positions + rb + t0 + r) != p0 + t0 + r;
     const int jp_check = p_max / p.P;
-    for (int jp = tid; jp <= max(jp_check, jp_last); jp += kTileM) {
+    for (int jp = tid; jp <= max(jp_check, jp_last); jp += NT) {
       const int pid = jp < p.max_blocks ? __ldg(bt + jp) : -1;
       if (jp <= jp_check) bad |= pid < 0 || pid >= p.num_pages;
       if (jp >= jp0 && jp <= jp_last) pids[jp - jp0] = pid;
@@ -229,7 +271,7 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
   // page ids -> tensor-map rows (pages past the sequence take the first page's)
   if (run) {
     const int fallback_pid = __ldg(bt + jp0);  // = pids[0], read where no thread overwrites it
-    for (int jp = jp0 + tid; jp <= jp_last; jp += kTileM) {
+    for (int jp = jp0 + tid; jp <= jp_last; jp += NT) {
       int pid = pids[jp - jp0];
       if (pid < 0 || pid >= p.num_pages) pid = fallback_pid;
       pids[jp - jp0] = (pid * p.Hkv + h) << lg_p;
@@ -238,248 +280,380 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
   __syncthreads();
 
   PrefillIssueLog log;
-  // ---- the ring: the three tile buffers take key and value tiles in the
-  // order the tensor pipe reads them, K(0), K(1), V(0), K(2), V(1), K(3), ...
-  // (item i in slot i % 3); a slot takes item i + 3 once the MMA that read
-  // item i is done, so a value tile is copied a key tile ahead of its P.V and
-  // a key tile about one ahead of its S.
-  auto item_tile = [](int i) { return i == 0 ? 0 : ((i & 1) ? (i + 1) / 2 : (i - 2) / 2); };
-  auto k_item = [](int jj) { return jj == 0 ? 0 : 2 * jj - 1; };
-  auto v_item = [](int jj) { return 2 * jj + 2; };
   const int lane = tid & 31;
-  auto issue_item = [&](int i) {  // all lanes of a loader warp; nothing past the CTA's key tiles
-    const int jj = item_tile(i);
-    if (jj >= nk) return;
-    const bool is_k = i == 0 || (i & 1);
-    prefill_load_kv<D>(is_k ? &p.kmap : &p.vmap, sm + (i % S::SLOTS) * S::TILE, &bar[BAR_R0 + i % S::SLOTS], pids, jp0,
-                       j_begin + jj, lg_p, lane);
-    if (lane == 0) last_item[i % S::SLOTS] = i;
-  };
-  auto wait_item = [&](int i) { return mbar_wait(&bar[BAR_R0 + i % S::SLOTS], (i / S::SLOTS) & 1, p.wait_limit); };
-  griddep_wait();  // the chunk's own rows, appended by a preceding dependent-launch append, are visible from here
-  if (warp == 0)
-    for (int i = 0; i < S::SLOTS; ++i) issue_item(i);
-  // Q row -> TMEM columns [T::Q, T::Q + D/2), two bf16 per column
-#pragma unroll
-  for (int c16 = 0; c16 < D / 32; ++c16) tc::tmem_st16(tb + lane_base + T::Q + c16 * 16, *reinterpret_cast<uint32_t(*)[16]>(&w[16 * c16]));
-  tc::tmem_wait_st();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-
   constexpr uint32_t id_qk = tc::idesc_bf16_f32(kTileM, kTileN, false);
   constexpr uint32_t id_pv = tc::idesc_bf16_f32(kTileM, D, true);
-  // S(jj) = Q K(jj)^T into S buffer jj % 2 (thread 0; K(jj) has landed)
-  auto issue_qk = [&](int jj) {
-    const unsigned char* K = sm + (k_item(jj) % S::SLOTS) * S::TILE;
+  // S(jj) = Q K(jj)^T into S buffer sb from the key tile at K (one thread;
+  // K(jj) has landed); completion arrives on bar[cb]
+  auto issue_qk = [&](const unsigned char* K, int cb, int sb) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const unsigned char* kb = K + (kk / 4) * S::KH + (kk % 4) * 32;
-      tc::mma_bf16_ts(tb + T::S + (jj & 1) * kTileN, tb + T::Q + kk * 8, tc::smem_desc(kb, 16, 1024), id_qk, kk > 0);
+      tc::mma_bf16_ts(tb + T::S + sb * kTileN, tb + T::Q + kk * 8, tc::smem_desc(kb, 16, 1024), id_qk, kk > 0);
     }
-    tc::mma_commit(&bar[BAR_S0 + (jj & 1)]);
-    log.issue(BAR_S0 + (jj & 1));
+    tc::mma_commit(&bar[cb]);
+    log.issue(cb);
   };
-  // O += P(jj) V(jj), P as (hi, lo) from S buffer jj % 2
-  auto issue_pv = [&](int jj) {
-    const unsigned char* Vt = sm + (v_item(jj) % S::SLOTS) * S::TILE;
+  // O += P(jj) V(jj), P as (hi, lo) from S buffer sb, V the tile at Vt
+  auto issue_pv = [&](int jj, const unsigned char* Vt, int cb, int sb) {
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
       const uint64_t vb = tc::smem_desc(Vt + kk * 2048, S::KH, 1024);  // 16 keys of the MN-major value tile
-      const uint32_t ph = tb + T::S + (jj & 1) * kTileN + (kk / 2) * 32 + (kk % 2) * 8;  // hi of keys 16kk .. +15; lo 16 columns on
+      const uint32_t ph = tb + T::S + sb * kTileN + (kk / 2) * 32 + (kk % 2) * 8;  // hi of keys 16kk .. +15; lo 16 columns on
       tc::mma_bf16_ts(tb + T::O, ph, vb, id_pv, jj > 0 || kk > 0);
       tc::mma_bf16_ts(tb + T::O, ph + 16, vb, id_pv, true);
     }
-    tc::mma_commit(&bar[BAR_O]);
-    log.issue(BAR_O);
+    tc::mma_commit(&bar[cb]);
+    log.issue(cb);
+  };
+  // Values past the chunk's last position may be stale or poisoned: zero
+  // those rows of a value tile so that 0-weights never meet a NaN (threads
+  // `first_thread` .. of a group of `nthreads`)
+  auto zero_tail = [&](unsigned char* Vt, int key0, int first_thread, int nthreads) {
+    const int first = max(0, p_last + 1 - key0);
+    const int n16 = (kTileN - first) * NH * 8;  // 16-byte pieces to clear
+    for (int i = first_thread; i < n16; i += nthreads) {
+      const int row = first + i / (NH * 8), piece = i % (NH * 8);
+      *reinterpret_cast<uint4*>(Vt + (piece / 8) * S::KH + row * 128 + (piece % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    tc::fence_proxy_async_smem();
   };
 
-  // Key tile j: S(j) done -> softmax(j) -> P.V(j).  Three threads issue the
-  // asynchronous work, each also a softmax row: thread 0 the copies, thread 32
-  // S(j+1) during softmax(j) (once P.V(j-1) has left the other S buffer and
-  // K(j+1) has landed), thread 64 P.V(j).  A tensor-core MMA of these shapes
-  // keeps its issuing thread about 100 cycles, so spreading the MMAs over two
-  // warps keeps either from holding back the block by a whole key tile.  The
-  // threads meet once per key tile, before P.V(j).  Every barrier has at most
-  // one phase outstanding; every wait is bounded.
-  constexpr int kLoader = 0, kSIssuer = 32, kPvIssuer = 64;  // threads
-  constexpr int kKWarp = 0, kVWarp = 3;                       // warps that issue key / value tile copies
+  // ---- the online softmax of this row's 64 scores of one key tile (log2
+  // domain), in two halves of 32 read from tensor memory twice (for the
+  // maximum, then for the weights), so that no more than 32 scores are live
+  // in registers.  The same code runs in both CTA shapes.
   float m_ref = -INFINITY, l_run = 0.0f;
-  bool ok = !(p.debug_stall && nk > 0) || mbar_wait(&bar[BAR_STALL], 0, p.wait_limit);  // the stall runs out
-  // a role thread's own waits; a failure there reaches the others at the next
-  // block-wide meeting (their waits on its work run out too: bounded)
-  bool role_ok = true;
-  if (tid == kSIssuer && nk > 0 && ok) {
-    role_ok = wait_item(k_item(0));
-    if (role_ok) {
-      tc::fence_after_sync();
-      issue_qk(0);
-    }
-  }
-  bool next_k_slot_refilled = false;  // warp 3: S(j)'s key slot already took its next item
-  for (int j = 0; j < nk && ok; ++j) {
-    // ---- S(j) done (each warp waits for itself)
-    bool good = __all_sync(0xffffffffu, mbar_wait(&bar[BAR_S0 + (j & 1)], (j >> 1) & 1, p.wait_limit));
-    tc::fence_after_sync();
-    // S(j) has read K(j): its slot takes the item three on, K(2) after S(0)
-    // (warp 0 issues key tiles), V(j) after S(j > 0) (warp 3 value tiles)
-    if (good && warp == (j == 0 ? kKWarp : kVWarp)) {
-      if (!next_k_slot_refilled) issue_item(k_item(j) + S::SLOTS);
-      next_k_slot_refilled = false;
-    }
-    if (good && tid == kSIssuer) log.seen(BAR_S0 + (j & 1));
-    const uint32_t col_s = tb + lane_base + T::S + (j & 1) * kTileN;
-    const int key0 = (j_begin + j) * kTileN;
-    float alpha = 1.0f;
-    // ---- online softmax of this row's 64 scores (log2 domain), in two halves of
-    // 32 read from tensor memory twice (for the maximum, then for the weights),
-    // so that no more than 32 scores are live in registers
-    const bool edge = key0 + kTileN - 1 > my_pos;  // the row's causal edge (or keys past the chunk) is in this tile
-    if (good) {
-      float mx = -INFINITY;
+  auto softmax_max = [&](uint32_t col_s, int key0, bool edge) -> float {  // returns the rescale factor
+    float mx = -INFINITY;
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        float sc[32];
-        tc::tmem_ld32(col_s + 32 * half, sc);
-        if (edge) {
+    for (int half = 0; half < 2; ++half) {
+      float sc[32];
+      tc::tmem_ld32(col_s + 32 * half, sc);
+      if (edge) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (key0 + 32 * half + i > my_pos) sc[i] = -INFINITY;
+        for (int i = 0; i < 32; ++i)
+          if (key0 + 32 * half + i > my_pos) sc[i] = -INFINITY;
+      }
+      float mx4[4] = {sc[0], sc[1], sc[2], sc[3]};
+#pragma unroll
+      for (int i = 4; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], sc[i]);
+      mx = fmaxf(mx, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])));
+    }
+    mx = __fmul_rn(mx, p.sm_scale_log2);  // the scale is positive: the largest scaled score is the scaled largest one
+    float alpha = 1.0f;
+    if (mx > __fadd_rn(m_ref, kRescaleSlack)) {
+      alpha = ex2(__fsub_rn(m_ref, mx));
+      m_ref = mx;
+      l_run = __fmul_rn(l_run, alpha);
+    }
+    return alpha;
+  };
+  auto softmax_weights = [&](uint32_t col_s, int key0, bool edge) {
+    // every score so far masked: the weights are ex2(-inf) = 0 against any finite reference
+    const float neg_ref = m_ref == -INFINITY ? 0.0f : -m_ref;
+    // weights -> (hi, lo) bf16 pairs in place of S: keys 32h .. 32h+31 as hi
+    // in columns 32h .. 32h+15 and lo in the 16 after them
+    float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      float sc[32];
+      tc::tmem_ld32(col_s + 32 * half, sc);
+      if (edge) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (key0 + 32 * half + i > my_pos) sc[i] = -INFINITY;
+      }
+#pragma unroll
+      for (int q8 = 0; q8 < 2; ++q8) {
+        uint32_t hw[8], lw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float a = ex2(fmaf(sc[16 * q8 + 2 * i], p.sm_scale_log2, neg_ref));
+          const float c = ex2(fmaf(sc[16 * q8 + 2 * i + 1], p.sm_scale_log2, neg_ref));
+          ls[i] = __fadd_rn(ls[i], __fadd_rn(a, c));
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(a, c);
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(__fsub_rn(a, __low2float(hi)), __fsub_rn(c, __high2float(hi)));
+          hw[i] = *reinterpret_cast<const uint32_t*>(&hi);
+          lw[i] = *reinterpret_cast<const uint32_t*>(&lo);
         }
-        float mx4[4] = {sc[0], sc[1], sc[2], sc[3]};
+        tc::tmem_st8(col_s + 32 * half + q8 * 8, hw);
+        tc::tmem_st8(col_s + 32 * half + 16 + q8 * 8, lw);
+      }
+    }
+    const float lsum = __fadd_rn(__fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3])),
+                                 __fadd_rn(__fadd_rn(ls[4], ls[5]), __fadd_rn(ls[6], ls[7])));
+    l_run = __fadd_rn(l_run, lsum);
+  };
+  // O *= alpha (the reference max moved; P.V(j-1), O's last writer, is done)
+  auto rescale_o = [&](float alpha) {
+#pragma unroll 1
+    for (int c4 = 0; c4 < D / 32; ++c4) {
+      float o[32];
+      tc::tmem_ld32(tb + lane_base + T::O + c4 * 32, o);
 #pragma unroll
-        for (int i = 4; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], sc[i]);
-        mx = fmaxf(mx, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])));
-      }
-      mx = __fmul_rn(mx, p.sm_scale_log2);  // the scale is positive: the largest scaled score is the scaled largest one
-      if (mx > __fadd_rn(m_ref, kRescaleSlack)) {
-        alpha = ex2(__fsub_rn(m_ref, mx));
-        m_ref = mx;
-        l_run = __fmul_rn(l_run, alpha);
-      }
+      for (int i = 0; i < 32; ++i) o[i] = __fmul_rn(o[i], alpha);
+      tc::tmem_st32(tb + lane_base + T::O + c4 * 32, o);
     }
-    // ---- P.V(j-1) done: warp 0 refills its value slot (with K(j+2)); thread
-    // 32 then issues S(j+1) into the other S buffer once K(j+1) has landed
-    if (good && role_ok && j > 0 && (warp == kKWarp || tid == kSIssuer)) {
-      role_ok = mbar_wait(&bar[BAR_O], (j - 1) & 1, p.wait_limit);
-      if (warp == kKWarp) {
-        role_ok = __all_sync(0xffffffffu, role_ok);
-        if (role_ok) issue_item(v_item(j - 1) + S::SLOTS);
-      }
+  };
+  // Q row -> TMEM columns [T::Q, T::Q + D/2), two bf16 per column (the
+  // softmax warps), then the block meets before the first MMA
+  auto q_to_tmem = [&]() {
+    if (warp < 4) {
+#pragma unroll
+      for (int c16 = 0; c16 < D / 32; ++c16)
+        tc::tmem_st16(tb + lane_base + T::Q + c16 * 16, *reinterpret_cast<uint32_t(*)[16]>(&w[16 * c16]));
+      tc::tmem_wait_st();
     }
-    if (good && role_ok && tid == kSIssuer && j + 1 < nk) {
-      role_ok = wait_item(k_item(j + 1));
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+  };
+
+  bool ok = !(p.debug_stall && nk > 0) || mbar_wait(&bar[kStall], 0, p.wait_limit);  // the stall runs out
+  if constexpr (!WS) {
+    // ---- the ring: the three tile buffers take key and value tiles in the
+    // order the tensor pipe reads them, K(0), K(1), V(0), K(2), V(1), K(3), ...
+    // (item i in slot i % 3); a slot takes item i + 3 once the MMA that read
+    // item i is done, so a value tile is copied a key tile ahead of its P.V and
+    // a key tile about one ahead of its S.
+    auto item_tile = [](int i) { return i == 0 ? 0 : ((i & 1) ? (i + 1) / 2 : (i - 2) / 2); };
+    auto k_item = [](int jj) { return jj == 0 ? 0 : 2 * jj - 1; };
+    auto v_item = [](int jj) { return 2 * jj + 2; };
+    auto issue_item = [&](int i) {  // all lanes of a loader warp; nothing past the CTA's key tiles
+      const int jj = item_tile(i);
+      if (jj >= nk) return;
+      const bool is_k = i == 0 || (i & 1);
+      prefill_load_kv<D>(is_k ? &p.kmap : &p.vmap, sm + (i % S::SLOTS) * S::TILE, &bar[BAR_R0 + i % S::SLOTS], pids,
+                         jp0, j_begin + jj, lg_p, lane);
+      if (lane == 0) last_item[i % S::SLOTS] = i;
+    };
+    auto wait_item = [&](int i) { return mbar_wait(&bar[BAR_R0 + i % S::SLOTS], (i / S::SLOTS) & 1, p.wait_limit); };
+    griddep_wait();  // the chunk's own rows, appended by a preceding dependent-launch append, are visible from here
+    if (warp == 0)
+      for (int i = 0; i < S::SLOTS; ++i) issue_item(i);
+    q_to_tmem();
+
+    // Key tile j: S(j) done -> softmax(j) -> P.V(j).  Three threads issue the
+    // asynchronous work, each also a softmax row: warps 0 and 3 the copies,
+    // thread 32 S(j+1) during softmax(j) (once P.V(j-1) has left the other S
+    // buffer and K(j+1) has landed), thread 64 P.V(j).  A tensor-core MMA of
+    // these shapes keeps its issuing thread about 100 cycles, so spreading the
+    // MMAs over two warps keeps either from holding back the block by a whole
+    // key tile.  The threads meet once per key tile, before P.V(j).  Every
+    // barrier has at most one phase outstanding; every wait is bounded.
+    constexpr int kLoader = 0, kSIssuer = 32, kPvIssuer = 64;  // threads
+    constexpr int kKWarp = 0, kVWarp = 3;                       // warps that issue key / value tile copies
+    // a role thread's own waits; a failure there reaches the others at the next
+    // block-wide meeting (their waits on its work run out too: bounded)
+    bool role_ok = true;
+    if (tid == kSIssuer && nk > 0 && ok) {
+      role_ok = wait_item(k_item(0));
       if (role_ok) {
         tc::fence_after_sync();
-        issue_qk(j + 1);
+        issue_qk(sm + (k_item(0) % S::SLOTS) * S::TILE, BAR_S0, 0);
       }
     }
-    if (good) {
-      // every score so far masked: the weights are ex2(-inf) = 0 against any finite reference
-      const float neg_ref = m_ref == -INFINITY ? 0.0f : -m_ref;
-      // weights -> (hi, lo) bf16 pairs in place of S: keys 32h .. 32h+31 as hi
-      // in columns 32h .. 32h+15 and lo in the 16 after them
-      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        float sc[32];
-        tc::tmem_ld32(col_s + 32 * half, sc);
-        if (edge) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (key0 + 32 * half + i > my_pos) sc[i] = -INFINITY;
-        }
-#pragma unroll
-        for (int q8 = 0; q8 < 2; ++q8) {
-          uint32_t hw[8], lw[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float a = ex2(fmaf(sc[16 * q8 + 2 * i], p.sm_scale_log2, neg_ref));
-            const float c = ex2(fmaf(sc[16 * q8 + 2 * i + 1], p.sm_scale_log2, neg_ref));
-            ls[i] = __fadd_rn(ls[i], __fadd_rn(a, c));
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(a, c);
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(__fsub_rn(a, __low2float(hi)), __fsub_rn(c, __high2float(hi)));
-            hw[i] = *reinterpret_cast<const uint32_t*>(&hi);
-            lw[i] = *reinterpret_cast<const uint32_t*>(&lo);
-          }
-          tc::tmem_st8(col_s + 32 * half + q8 * 8, hw);
-          tc::tmem_st8(col_s + 32 * half + 16 + q8 * 8, lw);
-        }
-      }
-      const float lsum = __fadd_rn(__fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3])),
-                                   __fadd_rn(__fadd_rn(ls[4], ls[5]), __fadd_rn(ls[6], ls[7])));
-      l_run = __fadd_rn(l_run, lsum);
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        // the reference max moved: rescale O (P.V(j-1), its last writer, is done:
-        // threads 0 and 32 saw it before S(j+1); the others see it here)
-        if (__all_sync(0xffffffffu, mbar_wait(&bar[BAR_O], (j - 1) & 1, p.wait_limit))) {
-          tc::fence_after_sync();
-#pragma unroll 1
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            float o[32];
-            tc::tmem_ld32(tb + lane_base + T::O + c4 * 32, o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __fmul_rn(o[i], alpha);
-            tc::tmem_st32(tb + lane_base + T::O + c4 * 32, o);
-          }
-        } else {
-          good = false;
-        }
-      }
-    }
-    tc::tmem_wait_st();
-    // ---- value tile: keys past the chunk's last position may hold stale or
-    // poisoned values; zero those rows so that 0-weights never meet a NaN
-    const int vi = v_item(j);
-    tc::fence_before_sync();
-    if (!(ok = __syncthreads_and(good && role_ok && wait_item(vi)))) break;
-    if (key0 + kTileN - 1 > p_last) {
-      unsigned char* Vt = sm + (vi % S::SLOTS) * S::TILE;
-      const int first = max(0, p_last + 1 - key0);
-      const int n16 = (kTileN - first) * NH * 8;  // 16-byte pieces to clear
-      for (int i = tid; i < n16; i += kTileM) {
-        const int row = first + i / (NH * 8), piece = i % (NH * 8);
-        *reinterpret_cast<uint4*>(Vt + (piece / 8) * S::KH + row * 128 + (piece % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      tc::fence_proxy_async_smem();
-      __syncthreads();
-    }
-    // ---- O += P V
-    if (tid == kPvIssuer) {
+    bool next_k_slot_refilled = false;  // warp 3: S(j)'s key slot already took its next item
+    for (int j = 0; j < nk && ok; ++j) {
+      // ---- S(j) done (each warp waits for itself)
+      bool good = __all_sync(0xffffffffu, mbar_wait(&bar[BAR_S0 + (j & 1)], (j >> 1) & 1, p.wait_limit));
       tc::fence_after_sync();
-      issue_pv(j);
-    }
-    if (warp == kVWarp && j + 1 < nk) {
-      // S(j+1) has usually finished by now: its key slot takes its next item
-      // (V(j+1)) a little earlier
-      if (__shfl_sync(0xffffffffu, mbar_test(&bar[BAR_S0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1) ? 1 : 0, 0)) {
-        issue_item(k_item(j + 1) + S::SLOTS);
-        next_k_slot_refilled = true;
+      // S(j) has read K(j): its slot takes the item three on, K(2) after S(0)
+      // (warp 0 issues key tiles), V(j) after S(j > 0) (warp 3 value tiles)
+      if (good && warp == (j == 0 ? kKWarp : kVWarp)) {
+        if (!next_k_slot_refilled) issue_item(k_item(j) + S::SLOTS);
+        next_k_slot_refilled = false;
+      }
+      if (good && tid == kSIssuer) log.seen(BAR_S0 + (j & 1));
+      const uint32_t col_s = tb + lane_base + T::S + (j & 1) * kTileN;
+      const int key0 = (j_begin + j) * kTileN;
+      const bool edge = key0 + kTileN - 1 > my_pos;  // the row's causal edge (or keys past the chunk) is in this tile
+      float alpha = 1.0f;
+      if (good) alpha = softmax_max(col_s, key0, edge);
+      // ---- P.V(j-1) done: warp 0 refills its value slot (with K(j+2)); thread
+      // 32 then issues S(j+1) into the other S buffer once K(j+1) has landed
+      if (good && role_ok && j > 0 && (warp == kKWarp || tid == kSIssuer)) {
+        role_ok = mbar_wait(&bar[BAR_O], (j - 1) & 1, p.wait_limit);
+        if (warp == kKWarp) {
+          role_ok = __all_sync(0xffffffffu, role_ok);
+          if (role_ok) issue_item(v_item(j - 1) + S::SLOTS);
+        }
+      }
+      if (good && role_ok && tid == kSIssuer && j + 1 < nk) {
+        role_ok = wait_item(k_item(j + 1));
+        if (role_ok) {
+          tc::fence_after_sync();
+          issue_qk(sm + (k_item(j + 1) % S::SLOTS) * S::TILE, BAR_S0 + ((j + 1) & 1), (j + 1) & 1);
+        }
+      }
+      if (good) {
+        softmax_weights(col_s, key0, edge);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          // threads 0 and 32 saw P.V(j-1) done before S(j+1); the others see it here
+          if (__all_sync(0xffffffffu, mbar_wait(&bar[BAR_O], (j - 1) & 1, p.wait_limit))) {
+            tc::fence_after_sync();
+            rescale_o(alpha);
+          } else {
+            good = false;
+          }
+        }
+      }
+      tc::tmem_wait_st();
+      const int vi = v_item(j);
+      tc::fence_before_sync();
+      if (!(ok = __syncthreads_and(good && role_ok && wait_item(vi)))) break;
+      if (key0 + kTileN - 1 > p_last) {
+        zero_tail(sm + (vi % S::SLOTS) * S::TILE, key0, tid, kTileM);
+        __syncthreads();
+      }
+      // ---- O += P V
+      if (tid == kPvIssuer) {
+        tc::fence_after_sync();
+        issue_pv(j, sm + (vi % S::SLOTS) * S::TILE, BAR_O, j & 1);
+      }
+      if (warp == kVWarp && j + 1 < nk) {
+        // S(j+1) has usually finished by now: its key slot takes its next item
+        // (V(j+1)) a little earlier
+        if (__shfl_sync(0xffffffffu, mbar_test(&bar[BAR_S0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1) ? 1 : 0, 0)) {
+          issue_item(k_item(j + 1) + S::SLOTS);
+          next_k_slot_refilled = true;
+        }
       }
     }
-  }
-  if (ok && nk > 0) {
-    // the last commit arrives when every MMA before it has completed too
-    ok = __syncthreads_and(mbar_wait(&bar[BAR_O], (nk - 1) & 1, p.wait_limit));
-    if (ok && tid == kPvIssuer) log.seen(BAR_O);
-  }
-  if (!ok) {
-    // every copy and MMA in flight finishes before TMEM or shared memory is
-    // reused: each MMA issuer drains its barriers; thread 0 the ring slots,
-    // whose loads two threads issue (each slot's last one, at most one in flight)
-    __syncthreads();
-    if (tid == kSIssuer || tid == kPvIssuer) log.drain(bar);
-    if (tid == kLoader) {
-      record_error(p.status, ST_TIMEOUT);
-      for (int r = 0; r < S::SLOTS; ++r)
-        if (last_item[r] >= 0) mbar_wait(&bar[BAR_R0 + r], (last_item[r] / S::SLOTS) & 1, kDrainWaitLimit);
+    if (ok && nk > 0) {
+      // the last commit arrives when every MMA before it has completed too
+      ok = __syncthreads_and(mbar_wait(&bar[BAR_O], (nk - 1) & 1, p.wait_limit));
+      if (ok && tid == kPvIssuer) log.seen(BAR_O);
+    }
+    if (!ok) {
+      // every copy and MMA in flight finishes before TMEM or shared memory is
+      // reused: each MMA issuer drains its barriers; thread 0 the ring slots,
+      // whose loads two warps issue (each slot's last one, at most one in flight)
+      __syncthreads();
+      if (tid == kSIssuer || tid == kPvIssuer) log.drain(bar, BAR_COUNT);
+      if (tid == kLoader) {
+        record_error(p.status, ST_TIMEOUT);
+        for (int r = 0; r < S::SLOTS; ++r)
+          if (last_item[r] >= 0) mbar_wait(&bar[BAR_R0 + r], (last_item[r] / S::SLOTS) & 1, kDrainWaitLimit);
+      }
+    }
+  } else {
+    // ---- warp-specialised: warps 0-3 are the softmax rows; warp 4 issues the
+    // key-tile copies (its lanes) and the S MMAs (lane 0), warp 5 the value-tile
+    // copies and the P.V MMAs.  Key tile j uses key and value buffer j % 3 and
+    // S buffer j % 3.  The warps never meet inside the loop; they wait on:
+    //   K(j) / V(j) landed
+    //   S(j) done        -> softmax(j) may read S; key buffer j % 3 is free
+    //   P(j) written     -> P.V(j) may run (one arrival per row)
+    //   P.V(j) done      -> S buffer j % 3 (P(j)) and value buffer j % 3 are
+    //                       free; O may be rescaled for key tile j + 1
+    // Every kind of barrier comes three to a kind, one per buffer, and key tile
+    // j + 3 can only reuse one after every waiter of key tile j has passed it:
+    // no waiter can mistake a later phase for its own.  A key or value tile is
+    // copied two key tiles ahead of its MMA.
+    constexpr int kSWarp = 4, kPvWarp = 5;
+    auto kbuf = [&](int jj) { return sm + (jj % 3) * S::TILE; };
+    auto vbuf = [&](int jj) { return sm + (3 + jj % 3) * S::TILE; };
+    auto par3 = [](int jj) { return static_cast<uint32_t>((jj / 3) & 1); };  // phase parity of key tile jj's barrier
+    griddep_wait();  // the chunk's own rows, appended by a preceding dependent-launch append, are visible from here
+    if (warp == kSWarp) {
+      for (int jj = 0; jj < 3 && jj < nk; ++jj) {
+        prefill_load_kv<D>(&p.kmap, kbuf(jj), &bar[WS_KF0 + jj], pids, jp0, j_begin + jj, lg_p, lane);
+        if (lane == 0) log.issue(WS_KF0 + jj);
+      }
+    } else if (warp == kPvWarp) {
+      for (int jj = 0; jj < 3 && jj < nk; ++jj) {
+        prefill_load_kv<D>(&p.vmap, vbuf(jj), &bar[WS_VF0 + jj], pids, jp0, j_begin + jj, lg_p, lane);
+        if (lane == 0) log.issue(WS_VF0 + jj);
+      }
+    }
+    q_to_tmem();
+    bool wok = ok;  // this warp's waits (warp-uniform)
+    if (warp == kSWarp) {
+      for (int j = 0; j < nk && wok; ++j) {
+        // S buffer j % 3 held P(j-3): P.V(j-3) must be done; K(j) landed
+        if (j >= 3) wok = __all_sync(0xffffffffu, mbar_wait(&bar[WS_OD0 + j % 3], par3(j - 3), p.wait_limit));
+        wok = wok && __all_sync(0xffffffffu, mbar_wait(&bar[WS_KF0 + j % 3], par3(j), p.wait_limit));
+        if (!wok) break;
+        if (lane == 0) {
+          log.seen(WS_KF0 + j % 3);
+          tc::fence_after_sync();
+          issue_qk(kbuf(j), WS_SD0 + j % 3, j % 3);
+        }
+        __syncwarp();
+        if (j + 2 < nk && j >= 1) {
+          // S(j-1) has read key buffer (j-1) % 3: it takes K(j+2)
+          wok = __all_sync(0xffffffffu, mbar_wait(&bar[WS_SD0 + (j - 1) % 3], par3(j - 1), p.wait_limit));
+          if (!wok) break;
+          if (lane == 0) log.seen(WS_SD0 + (j - 1) % 3);
+          prefill_load_kv<D>(&p.kmap, kbuf(j + 2), &bar[WS_KF0 + (j + 2) % 3], pids, jp0, j_begin + j + 2, lg_p, lane);
+          if (lane == 0) log.issue(WS_KF0 + (j + 2) % 3);
+        }
+      }
+    } else if (warp == kPvWarp) {
+      for (int j = 0; j < nk && wok; ++j) {
+        wok = __all_sync(0xffffffffu, mbar_wait(&bar[WS_PR0 + j % 3], par3(j), p.wait_limit) &&
+                                           mbar_wait(&bar[WS_VF0 + j % 3], par3(j), p.wait_limit));
+        if (!wok) break;
+        if (lane == 0) log.seen(WS_VF0 + j % 3);
+        const int key0 = (j_begin + j) * kTileN;
+        if (key0 + kTileN - 1 > p_last) {
+          zero_tail(vbuf(j), key0, lane, 32);
+          __syncwarp();
+        }
+        if (lane == 0) {
+          tc::fence_after_sync();
+          issue_pv(j, vbuf(j), WS_OD0 + j % 3, j % 3);
+        }
+        __syncwarp();
+        if (j + 2 < nk && j >= 1) {
+          // P.V(j-1) has read value buffer (j-1) % 3: it takes V(j+2)
+          wok = __all_sync(0xffffffffu, mbar_wait(&bar[WS_OD0 + (j - 1) % 3], par3(j - 1), p.wait_limit));
+          if (!wok) break;
+          if (lane == 0) log.seen(WS_OD0 + (j - 1) % 3);
+          prefill_load_kv<D>(&p.vmap, vbuf(j + 2), &bar[WS_VF0 + (j + 2) % 3], pids, jp0, j_begin + j + 2, lg_p, lane);
+          if (lane == 0) log.issue(WS_VF0 + (j + 2) % 3);
+        }
+      }
+    } else {
+      for (int j = 0; j < nk && wok; ++j) {
+        wok = __all_sync(0xffffffffu, mbar_wait(&bar[WS_SD0 + j % 3], par3(j), p.wait_limit));
+        if (!wok) break;
+        tc::fence_after_sync();
+        const uint32_t col_s = tb + lane_base + T::S + (j % 3) * kTileN;
+        const int key0 = (j_begin + j) * kTileN;
+        const bool edge = key0 + kTileN - 1 > my_pos;  // the row's causal edge (or keys past the chunk) is in this tile
+        const float alpha = softmax_max(col_s, key0, edge);
+        softmax_weights(col_s, key0, edge);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          wok = __all_sync(0xffffffffu, mbar_wait(&bar[WS_OD0 + (j - 1) % 3], par3(j - 1), p.wait_limit));
+          if (!wok) break;
+          tc::fence_after_sync();
+          rescale_o(alpha);
+        }
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        mbar_arrive(&bar[WS_PR0 + j % 3]);
+      }
+      // the last P.V (its commit arrives when every MMA before it is done too)
+      if (wok && nk > 0)
+        wok = __all_sync(0xffffffffu, mbar_wait(&bar[WS_OD0 + (nk - 1) % 3], par3(nk - 1), p.wait_limit));
+    }
+    ok = __syncthreads_and(wok);
+    if (!ok) {
+      // every copy and MMA in flight finishes before TMEM or shared memory is
+      // reused: lane 0 of each issuing warp drains what it issued
+      if (lane == 0 && (warp == kSWarp || warp == kPvWarp)) log.drain(bar, WS_COUNT);
+      if (tid == 0) record_error(p.status, ST_TIMEOUT);
     }
   }
   __syncthreads();
+  const bool row_thread = warp < 4;  // the threads that own a TMEM lane (every thread of the decode-shaped CTA)
   if (nk > 0) {
     tc::fence_after_sync();
     if (nsplit == 1) {
-      if (ok) {
+      if (ok && row_thread) {
         const float inv = __fdiv_rn(1.0f, l_run);
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + row_off;
 #pragma unroll 1
@@ -514,24 +688,26 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
       const int ti = p.chunk_tile_begin[c] + mt * p.Hkv + h;  // the tile (its counter)
       const size_t blk0 = static_cast<size_t>(ti) * p.tile_splits;
       float* po = p.ws_tile_o + (blk0 + split) * (kTileM * D);
+      if (row_thread) {
 #pragma unroll 1
-      for (int c4 = 0; c4 < D / 32; ++c4) {
-        float o[32];
-        if (ok) {
-          tc::tmem_ld32(tb + lane_base + T::O + c4 * 32, o);
-        } else {
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          float o[32];
+          if (ok) {
+            tc::tmem_ld32(tb + lane_base + T::O + c4 * 32, o);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0.0f;
-        }
+            for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+          }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int col = c4 * 32 + 4 * i;
-          float4* dst = reinterpret_cast<float4*>(po + (col / CB) * (kTileM * CB)) + ((col % CB) / 4) * kTileM + m;
-          *dst = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          for (int i = 0; i < 8; ++i) {
+            const int col = c4 * 32 + 4 * i;
+            float4* dst = reinterpret_cast<float4*>(po + (col / CB) * (kTileM * CB)) + ((col % CB) / 4) * kTileM + m;
+            *dst = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          }
         }
+        reinterpret_cast<float2*>(p.ws_tile_ml)[(blk0 + split) * kTileM + m] =
+            make_float2(ok ? m_ref : -INFINITY, ok ? l_run : 0.0f);
       }
-      reinterpret_cast<float2*>(p.ws_tile_ml)[(blk0 + split) * kTileM + m] =
-          make_float2(ok ? m_ref : -INFINITY, ok ? l_run : 0.0f);
       __threadfence();
       __syncthreads();
       int32_t* counter = p.ws_tile_count + ti;
@@ -548,7 +724,7 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
         const float* pbase = p.ws_tile_o + blk0 * (kTileM * D);
         const int nb = NBS * nsplit;
         auto issue_block = [&](int b) {  // block b: column block b / nsplit of key range b % nsplit
-          uint64_t* mb = &bar[BAR_M0 + b % kMergeSlots];
+          uint64_t* mb = &bar[kM0 + b % kMergeSlots];
           mbar_arrive_expect_tx(mb, static_cast<uint32_t>(S::TILE));
           bulk_g2s(sm + (b % kMergeSlots) * S::TILE,
                    pbase + static_cast<size_t>(b % nsplit) * (kTileM * D) + (b / nsplit) * (kTileM * CB),
@@ -559,13 +735,14 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
           fence_proxy_async_global();  // the other CTAs' partials, seen through the counter, before the bulk reads
           for (; issued < min(kMergeSlots, nb); ++issued) issue_block(issued);
         }
+        const int mr = row_thread ? m : 0;  // the issuing warps of the wider CTA own no row: they read row 0
         float M = -INFINITY;
 #pragma unroll 4
-        for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(mlt + sp * kTileM + m).x);
+        for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(mlt + sp * kTileM + mr).x);
         float lsum = 0.0f;
 #pragma unroll 4
         for (int sp = 0; sp < nsplit; ++sp) {
-          const float2 v = __ldcg(mlt + sp * kTileM + m);
+          const float2 v = __ldcg(mlt + sp * kTileM + mr);
           lsum = fmaf(ex2(__fsub_rn(v.x, M)), v.y, lsum);
         }
         const float inv = __fdiv_rn(1.0f, lsum);
@@ -578,11 +755,11 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
 #pragma unroll 1
           for (int sp = 0; sp < nsplit; ++sp) {
             const int b = cb * nsplit + sp;
-            const float mv = __ldcg(mlt + sp * kTileM + m).x;
-            const bool got = mbar_wait(&bar[BAR_M0 + b % kMergeSlots], (b / kMergeSlots) & 1, p.wait_limit);
+            const float mv = __ldcg(mlt + sp * kTileM + mr).x;
+            const bool got = mbar_wait(&bar[kM0 + b % kMergeSlots], (b / kMergeSlots) & 1, p.wait_limit);
             if (got) {
               const float f = ex2(__fsub_rn(mv, M));
-              const float4* src = reinterpret_cast<const float4*>(sm + (b % kMergeSlots) * S::TILE) + m;
+              const float4* src = reinterpret_cast<const float4*>(sm + (b % kMergeSlots) * S::TILE) + mr;
 #pragma unroll
               for (int i = 0; i < CB / 4; ++i) {
                 const float4 v = src[i * kTileM];
@@ -616,7 +793,7 @@ __device__ __forceinline__ void prefill_tile(const AttnParams& p, int cta, unsig
         if (!mok && tid == 0) {
           record_error(p.status, ST_TIMEOUT);
           for (int b = max(0, issued - kMergeSlots); b < issued; ++b)  // copies in flight land before the CTA leaves
-            mbar_wait(&bar[BAR_M0 + b % kMergeSlots], (b / kMergeSlots) & 1, kDrainWaitLimit);
+            mbar_wait(&bar[kM0 + b % kMergeSlots], (b / kMergeSlots) & 1, kDrainWaitLimit);
         }
         if (tid == 0) *counter = 0;  // leave the workspace zero-filled for the next call
       }

@@ -125,3 +125,81 @@ def test_tile_path_timeout_reports_and_recovers():
     torch.cuda.synchronize()
     assert int(st.status.item()) == 0
     assert torch.equal(st.out.view(torch.int16), good)
+
+
+def chunk_alone(st, wl, c=0):
+    """Chunk c of the workload attended in a call of its own (only tile-path
+    rows: the launch of tile CTAs alone)."""
+    b, n = wl.chunks[c]
+    sl = slice(b, b + n)
+    out = torch.empty_like(st.q[sl])
+    wsb = pa.workspace_bytes(st.pool, n, wl.Hq, wl.max_blocks, [(0, n)])
+    ws = torch.zeros(max(wsb, 1), dtype=torch.uint8, device="cuda")
+    st.status.zero_()
+    pa.attention(st.pool, st.q[sl].contiguous(), st.seq_ids[sl].contiguous(), st.positions[sl].contiguous(),
+                 st.block_tables, out, chunks=[(0, n)], softmax_scale=wl.softmax_scale, workspace=ws, status=st.status)
+    torch.cuda.synchronize()
+    return out, sl
+
+
+@pytest.mark.parametrize("shape", [
+    dict(G=2, D=128, P=32, chunk=(300, 200, 600)),
+    dict(G=7, D=128, P=16, chunk=(0, 130, 150)),
+    dict(G=1, D=64, P=64, chunk=(37, 64, 200)),
+    dict(G=8, D=128, P=128, chunk=(64, 257, 321)),
+    dict(G=4, D=64, P=256, chunk=(9000, 200, 9300)),   # key ranges split and merged
+    dict(G=2, D=128, P=16, chunk=(9000, 200, 9300)),
+], ids=lambda d: f"G{d['G']}-D{d['D']}-P{d['P']}-at{d['chunk'][0]}")
+def test_tiles_only_launch_bits_equal_mixed_launch(shape):
+    """A call whose rows are all in a tile-path chunk runs the tile CTAs in a
+    launch of their own shape; the chunk rows' bits must equal those the same
+    rows get beside decode rows, and match the oracle."""
+    G, D, P = shape["G"], shape["D"], shape["P"]
+    wl = W.chunked_step(80 + G + D + P, [shape["chunk"]], decode_ctx=[30, 700], Hq=2 * G, Hkv=2, D=D, P=P)
+    st = pa_setup.upload(wl)
+    st.append_step()
+    st.attend()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    mixed = st.out.view(torch.int16).clone()
+    out, sl = chunk_alone(st, wl)
+    assert int(st.status.item()) == 0
+    assert torch.equal(out.view(torch.int16), mixed[sl]), "chunk rows differ between the two launches"
+    kp, vp = oracle_pools(wl)
+    ref = oracle_out(wl, kp, vp)[sl]
+    got = W.bf16_bits_to_f32(pa_setup.to_numpy(out)).astype(np.float64)
+    assert_close(got, ref, wl, "chunk alone")
+
+
+def test_tiles_only_launch_step_and_timeout():
+    """pa_step on a call of chunk rows only (the append, then the tile launch
+    as its dependent) equals the two calls; an injected stall in the tile
+    launch reports PA_ERR_TIMEOUT and the next call is exact again."""
+    wl = W.chunked_step(91, [(500, 256, 800)])
+    a = pa_setup.upload(wl)
+    a.append_step()
+    a.attend()
+    b = pa_setup.upload(wl)
+    b.step()
+    torch.cuda.synchronize()
+    assert int(a.status.item()) == 0 and int(b.status.item()) == 0
+    assert torch.equal(a.k_pool.view(torch.int16), b.k_pool.view(torch.int16))  # NaN-poisoned slots: compare bits
+    assert torch.equal(a.v_pool.view(torch.int16), b.v_pool.view(torch.int16))
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    good = a.out.view(torch.int16).clone()
+    pa.set_wait_limit(1000)
+    pa.debug_stall_waits(True)
+    try:
+        a.status.zero_()
+        a.attend()
+        torch.cuda.synchronize()
+        code = int(a.status.item())
+    finally:
+        pa.debug_stall_waits(False)
+        pa.set_wait_limit(0)
+    assert code == pa.PA_ERR_TIMEOUT
+    a.status.zero_()
+    a.attend()
+    torch.cuda.synchronize()
+    assert int(a.status.item()) == 0
+    assert torch.equal(a.out.view(torch.int16), good)
