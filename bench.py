@@ -81,7 +81,8 @@ def measured_bf16_tflops():
 
 def prefill_tiles_alone(pa, torch, st, wl, steps: int, stream):
     """The chunk rows of the step attended alone (one launch of prefill tiles
-    only, after the step's append): tensor-pipe fraction of the tiles.
+    only, after the step's append: the warp-specialised tile CTAs, whose
+    chunk rows have the mixed launch's bits): tensor-pipe fraction of the tiles.
     Algorithmic FLOPs: 4 * D per (chunk row, visible key, query head) --
     Q.K and P.V, one multiply-add each."""
     import numpy as np
@@ -112,7 +113,7 @@ def prefill_tiles_alone(pa, torch, st, wl, steps: int, stream):
     peak, kind = measured_bf16_tflops()
     tflops = flops / (ms / 1e3) / 1e12
     return {"gflop": flops / 1e9, "ms": ms, "tflops": tflops, "peak_tflops": peak, "frac": tflops / peak,
-            "peak_source": f"{kind} (MEASURED_PEAKS.json bf16_tflops, burst)", "kernel": "mixed_kernel tiles only"}
+            "peak_source": f"{kind} (MEASURED_PEAKS.json bf16_tflops, burst)", "kernel": "prefill_kernel (chunk tiles only)"}
 
 
 def profiled_traffic(workload: str, src_hash: str):
