@@ -14,7 +14,9 @@
 //   * A CTA is ONE warp.  A unit's work is a short chain (a few stages at the
 //     context lengths of a 7B-class decode batch), so many small CTAs per SM
 //     keep more units' copies in flight than a few wide ones, and no
-//     cross-warp merge is needed.  The warp waits on, consumes and refills
+//     cross-warp merge is needed.  (Opt-in row groups put 2, 4 or 8 such
+//     units in one CTA to share the copies of a common prefix: see
+//     decode_mma_group_kernel below.)  The warp waits on, consumes and refills
 //     its ring of NST slots in stage order; NST (2, 4 or 8) follows the
 //     number of units in the launch.
 //   * Stages of 32 tokens arrive by 2-D tensor-map copies (box: 128 bytes x

@@ -7,7 +7,9 @@
 // units no occupancy.  The decode rows run the same units as in a decode-only
 // launch, so their bits do not depend on a chunk being present: the SIMT units
 // for G <= 2 or D = 64, the tensor-core units (on the CTA's first warp; the
-// others leave at once) for D = 128 and G >= 3.
+// others leave at once) for D = 128 and G >= 3.  A call whose rows are all
+// chunk tiles takes the warp-specialised tile launch instead
+// (pa_prefill_bf16.cu), with the same per-row arithmetic.
 #include "pa_decode.cuh"
 #include "pa_decode_mma_bf16.cuh"
 #include "pa_prefill.cuh"

@@ -14,21 +14,27 @@
 //                        pair, V from shared memory, FP32 accumulator in TMEM
 // over key tiles of 64 keys, then O / l rounded to BF16.
 //
-// The CTA has the decode unit's shape (4 warps, about 50 KB of shared memory,
-// at most 128 registers a thread) so that tiles and decode units share one
-// launch without lowering the decode occupancy.  Shared memory holds two key
-// tiles and one value tile (128-byte swizzled, loaded by 2-D tensor-map copies
-// of one page x 64 head elements each; no multicast) and the page ids of the
-// CTA's key range, read from the block table once.  Tensor memory (256
-// columns, so that two tile CTAs share an SM and one's softmax overlaps the
-// other's MMAs) holds S of the current key tile, then P of it in place, Q and
-// O.  Thread m owns TMEM lane m = tile row m; thread 0 alone issues copies and
-// MMAs.  Schedule of key tile j: P.V(j-1) done -> V(j) into the value buffer,
-// S(j) issued (K(j) landed a key tile earlier) -> S(j) done: its key buffer
-// takes K(j+2) -> softmax, one read of the 64 scores from tensor memory ->
-// P.V(j).  A tile's key range is split across CTAs in fixed pieces of
-// kTileSplitKeys keys, merged in ascending order.  Every barrier has at most
-// one phase outstanding; every wait is bounded.
+// Two CTA shapes run the same per-row arithmetic, so a chunk row's bits do
+// not depend on which one ran it:
+//   * in a launch that also runs decode units, the tile CTA has the decode
+//     unit's shape (4 warps, about 51 KB of shared memory, at most 128
+//     registers a thread) so that mixing lowers no decode occupancy.  Three
+//     tile buffers form one ring that takes key and value tiles in the order
+//     the MMAs read them; two S buffers let S(j+1) run while the threads turn
+//     S(j) into P(j); four threads in four warps issue the copies and MMAs
+//     (an MMA of these shapes holds its issuing thread ~100 cycles); the block
+//     meets once per key tile, before P.V(j);
+//   * in a launch of chunk tiles only, the CTA is warp-specialised: four
+//     softmax warps and two issuing warps (key copies + S MMAs, value copies +
+//     P.V MMAs), three S buffers and three key and three value buffers, and
+//     the roles synchronise through mbarriers only.
+// Tiles are 2-D tensor-map copies of one page x 64 head elements (128-byte
+// swizzle, no multicast), the tensor-map row of each page of the CTA's key
+// range computed once from the block table.  TMEM (512 columns) holds the S
+// buffers (P in place), Q and O; thread m owns TMEM lane m = tile row m.  A
+// tile's key range is split across CTAs in fixed pieces of kTileSplitKeys
+// keys, merged in ascending order by the last CTA of the tile.  Every barrier
+// has at most one phase outstanding; every wait is bounded.
 //
 // Precision: the scores and the softmax are FP32.  Each weight p enters the
 // P.V product as hi = bf16(p) and lo = bf16(p - hi), so the product sees p to
