@@ -469,6 +469,28 @@ def row_groups_entry(env, steps: int, warmup: int):
     return out
 
 
+def long_prefill_entry(env, steps: int, warmup: int):
+    """A prefill step of one 4096-token causal chunk: 512 tiles on the
+    tensor-core path (the launch of chunk tiles only), enough to occupy every
+    SM.  Algorithmic FLOPs: 4 * D per (row, visible key, query head)."""
+    import numpy as np
+    torch, pa, W = env.torch, env.pa, env.W
+    wl = W.long_prefill()
+    st = env.pa_setup.upload(wl, device=env.dev)
+    t = time_steps(env, st, wl, steps, warmup)
+    flops = 4.0 * wl.D * wl.Hq * float(np.sum(wl.positions.astype(np.int64) + 1))
+    peak, kind = measured_bf16_tflops()
+    tflops = flops / (t["attention_ms"] / 1e3) / 1e12
+    out = {"workload": wl.description, "rows": wl.n_rows, "gflop": flops / 1e9, "attention_ms": t["attention_ms"],
+           "ms_per_step": t["ms_per_step"], "tflops": tflops, "peak_tflops": peak, "frac": tflops / peak,
+           "peak_source": f"{kind} (MEASURED_PEAKS.json bf16_tflops, burst)",
+           "kernel": "prefill_kernel (chunk tiles only)", "gpu_launches": t["launches"], "clocks": t["clocks"]}
+    del st
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -594,6 +616,7 @@ def run_ours(args):
         for name in ALL_WORKLOADS:
             entries[name] = workload_entry(env, name, max(args.steps, 20), max(args.warmup, 3))
         entries["shared_prefix_row_groups"] = row_groups_entry(env, max(args.steps, 20), max(args.warmup, 3))
+        entries["long_prefill"] = long_prefill_entry(env, max(args.steps, 20), max(args.warmup, 3))
 
     if rank == 0:
         line = {

@@ -203,3 +203,20 @@ def test_tiles_only_launch_step_and_timeout():
     torch.cuda.synchronize()
     assert int(a.status.item()) == 0
     assert torch.equal(a.out.view(torch.int16), good)
+
+
+def test_long_prefill_sampled_rows():
+    """The prefill-step workload of the benchmark (one 4096-token causal chunk,
+    512 tiles, no decode rows): pool bytes equal the oracle's; rows sampled
+    across the chunk (tile edges, the first and last rows) match the oracle."""
+    wl = W.long_prefill()
+    st = pa_setup.upload(wl)
+    st.step()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    kp, vp = oracle_pools(wl)
+    assert pa_setup.to_numpy(st.k_pool).tobytes() == kp.tobytes()
+    assert pa_setup.to_numpy(st.v_pool).tobytes() == vp.tobytes()
+    rows = np.array([0, 1, 63, 64, 65, 127, 128, 1000, 2047, 2048, 3071, 4031, 4032, 4094, 4095])
+    got = W.bf16_bits_to_f32(pa_setup.to_numpy(st.out)[rows]).astype(np.float64)
+    assert_close(got, oracle_out(wl, kp, vp, rows=rows), wl, "long prefill, sampled rows")

@@ -467,6 +467,17 @@ def chunked_step(seed: int, chunks, decode_ctx=(), Hq: int = 16, Hkv: int = 8, D
                     chunks=spans, description=f"chunked step: {n_dec} decode rows + chunks {list(chunks)}")
 
 
+def long_prefill(seed: int = 6, n_tokens: int = 4096, Hq: int = 16, Hkv: int = 8, D: int = 128,
+                 P: int = 32) -> Workload:
+    """A prefill step: one sequence's first n_tokens tokens as one causal chunk
+    (no decode rows), the head shape of the mixed step."""
+    wl = chunked_step(seed, [(0, n_tokens, n_tokens)], Hq=Hq, Hkv=Hkv, D=D, P=P)
+    wl.name = "long_prefill"
+    wl.description = (f"prefill step: one {n_tokens}-token causal chunk, Hq{Hq}/Hkv{Hkv}, D{D}, bf16, P{P}, "
+                      f"no decode rows")
+    return wl
+
+
 CONFIGS = {
     "tiny_decode": tiny_decode,
     "batched_decode": batched_decode,
