@@ -200,6 +200,8 @@ class ClockSampler:
 
 def make_workload(name: str, seqs: int = 0):
     import workloads as W
+    if name == "long_prefill":  # a prefill step (not a headline config): the tile path at full-GPU size
+        return W.long_prefill()
     if seqs > 0:
         if name in ("batched_decode", "batched_decode_fp8", "long_context", "long_context_fp8"):
             return W.CONFIGS[name](n_seqs=seqs)
@@ -301,6 +303,9 @@ def attention_kernel_name(wl) -> str:
     import workloads as W
     G = wl.Hq // wl.Hkv
     if wl.chunks and wl.kv_dtype == W.BF16 and wl.q_dtype == W.BF16:
+        # every row in a chunk: the launch of chunk tiles only
+        if sum(n for _, n in wl.chunks) == wl.n_rows and min(n for _, n in wl.chunks) >= 16:
+            return "prefill_kernel"
         return "mixed_kernel"
     if wl.kv_dtype == W.E4M3 and wl.D == 128 and 1 <= G <= 8 and wl.q_dtype == W.BF16:
         return "decode_mma_kernel"
@@ -657,7 +662,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="batched_decode",
-                    choices=sorted(W_CONFIG_NAMES))
+                    choices=sorted(W_CONFIG_NAMES) + ["long_prefill"])
     ap.add_argument("--seqs", type=int, default=0, help="shrink the workload to this many sequences (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
