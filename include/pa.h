@@ -134,9 +134,10 @@ pa_status pa_append_kv(const pa_pool *pool, int32_t n_rows, const void *k_new, c
 
 /* Workspace bytes pa_attention needs for these rows, this block-table width
  * and these prefill chunks (the split-KV partial triples of decode rows and of
- * chunk tiles, and their counters).  0 when nothing can be split.  Computed on
- * the host from sizes only; for a bf16 pool it assumes the chunks take the
- * tensor-core tile path (bf16 queries), which never needs less. */
+ * chunk tiles, their counters, and the decode rows' launch order when
+ * pa_set_unit_order asks for one).  0 when nothing can be split or ordered.
+ * Computed on the host from sizes only; for a bf16 pool it assumes the chunks
+ * take the tensor-core tile path (bf16 queries), which never needs less. */
 size_t pa_attention_workspace_bytes(const pa_pool *pool, int32_t n_rows, int32_t num_q_heads,
                                     int32_t max_blocks_per_seq, const pa_chunk *chunks, int32_t n_chunks);
 
@@ -147,16 +148,19 @@ size_t pa_attention_workspace_bytes(const pa_pool *pool, int32_t n_rows, int32_t
  *                at most 16 chunks.  Rows not in a chunk are decode rows.
  *   softmax_scale <= 0 selects 1 / sqrt(head_dim)
  *   workspace    device memory of at least pa_attention_workspace_bytes(...), 256-byte
- *                aligned, ZERO-FILLED BEFORE ITS FIRST USE; every call leaves it
- *                zero-filled again, so it is reused without clearing (except after a call
- *                that reported PA_ERR_TIMEOUT: clear it again).  Calls that share a
- *                workspace must not overlap on the GPU.  May be NULL when 0 bytes are needed.
+ *                aligned, ZERO-FILLED BEFORE ITS FIRST USE; every call leaves the split
+ *                counters in it at zero again, so it is reused without clearing (except
+ *                after a call that reported PA_ERR_TIMEOUT: clear it again); the other
+ *                bytes are scratch that each call writes before it reads them.  Calls that
+ *                share a workspace must not overlap on the GPU.  May be NULL when 0 bytes
+ *                are needed.
  * Each row attends keys 0..positions[r] of its own sequence (its own token
  * included, so append the step's rows first).  A row's output bits depend only
  * on that row's inputs and on the rows of its own chunk, never on the other
  * rows of the call or the physical placement of its pages.
- * One launch on `stream` (split partials are merged inside it); no allocation;
- * graph-capturable.  Errors: PA_ERR_INVALID_ARG (NULL or misaligned pointer,
+ * One launch on `stream` (split partials are merged inside it), preceded by
+ * the one-CTA launch that orders the decode rows when pa_set_unit_order says
+ * so; no allocation; graph-capturable.  Errors: PA_ERR_INVALID_ARG (NULL or misaligned pointer,
  * bad sizes, overlapping chunks, workspace too small), PA_ERR_UNSUPPORTED (a
  * group size or head_dim without a kernel), PA_ERR_CUDA (a failed launch). */
 pa_status pa_attention(const pa_pool *pool, int32_t n_rows, const void *q, pa_dtype q_dtype,
@@ -250,6 +254,27 @@ int32_t pa_get_split_tokens(void);
  * other than 1, 2, 4 or 8. */
 pa_status pa_set_row_groups(int32_t rows);
 int32_t pa_get_row_groups(void);
+
+/* Launch order of the decode rows.  A decode launch runs one CTA per (row,
+ * split, kv head) and the GPU starts CTAs roughly in index order, so a long
+ * row listed late starts in the last wave and runs on after the rest of the
+ * launch has finished.  PA_ORDER_LONGEST_FIRST runs the units of the rows
+ * with the most keys per unit first ("llm-rs ...", section "2. Why decode is
+ * a memory problem": keep HBM busy to the end of the launch): one CTA, of a
+ * launch of its own or of pa_step's append launch, sorts the rows by the key
+ * count of their longest unit into the workspace, and the attention launch
+ * reads the order (its programmatic dependent).  PA_ORDER_CALL keeps the
+ * call's order, one launch fewer.  PA_ORDER_AUTO (the default) orders a call
+ * of at least 128 decode rows whose units can hold 1024 keys or more
+ * (max_blocks_per_seq * page_size and the split length both at least 1024),
+ * and keeps the order of other calls.  Output bits never depend on it: a
+ * row's arithmetic is the same wherever it runs.  Row groups (rows > 1 above)
+ * keep the call's order.  A process-wide setting, read once per call like the
+ * split length; the workspace size depends on it.  Returns PA_ERR_INVALID_ARG
+ * for another value. */
+enum { PA_ORDER_AUTO = 0, PA_ORDER_CALL = 1, PA_ORDER_LONGEST_FIRST = 2 };
+pa_status pa_set_unit_order(int32_t mode);
+int32_t pa_get_unit_order(void);
 
 /* Longest time, in microseconds, one device-side wait (for a copy or an MMA
  * to complete) may take before it gives up with PA_ERR_TIMEOUT; 0 restores

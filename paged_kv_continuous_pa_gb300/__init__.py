@@ -20,6 +20,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "pa.h")
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE, PA_ERR_TIMEOUT, PA_ERR_CUDA, PA_ERR_NO_PAGES = range(7)
 PA_ADMIT_OK, PA_ADMIT_NO_PAGES, PA_ADMIT_TOO_LONG, PA_ADMIT_SEQ_IN_USE, PA_ADMIT_BAD_ARG = range(5)
 PA_F32, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
+PA_ORDER_AUTO, PA_ORDER_CALL, PA_ORDER_LONGEST_FIRST = 0, 1, 2
 
 _lib = None
 _lock = threading.Lock()
@@ -107,6 +108,10 @@ def load(path: str = LIB_PATH):
         L.pa_set_row_groups.restype = st
         L.pa_get_row_groups.argtypes = []
         L.pa_get_row_groups.restype = i32
+        L.pa_set_unit_order.argtypes = [i32]
+        L.pa_set_unit_order.restype = st
+        L.pa_get_unit_order.argtypes = []
+        L.pa_get_unit_order.restype = i32
         L.pa_set_wait_limit.argtypes = [ctypes.c_uint32]
         L.pa_set_wait_limit.restype = None
         L.pa_debug_stall_waits.argtypes = [i32]
@@ -371,6 +376,14 @@ def set_row_groups(rows: int):
 
 def get_row_groups() -> int:
     return int(load().pa_get_row_groups())
+
+
+def set_unit_order(mode: int):
+    _check(load().pa_set_unit_order(int(mode)))
+
+
+def get_unit_order() -> int:
+    return int(load().pa_get_unit_order())
 
 
 def set_wait_limit(microseconds: int):

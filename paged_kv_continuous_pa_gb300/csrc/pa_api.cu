@@ -1,5 +1,6 @@
 // pa_api.cu -- the C ABI declared in include/pa.h: argument validation, launch
 // geometry and dispatch.  No allocation, no device synchronisation.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -40,6 +41,7 @@ thread_local char g_last_error[512] = "";
 // process-wide settings; any thread may change them, and a call reads each once
 std::atomic<int32_t> g_split_tokens{pa::kDefaultSplitTokens};
 std::atomic<int32_t> g_row_groups{1};
+std::atomic<int32_t> g_unit_order{PA_ORDER_AUTO};
 std::atomic<uint32_t> g_wait_limit{pa::kDefaultWaitLimit};
 std::atomic<int32_t> g_debug_stall{0};
 
@@ -77,12 +79,25 @@ struct Plan {
   int row_begin[pa::kMaxChunks];
   int tile_begin[pa::kMaxChunks];
   int total_tiles = 0, total_rows = 0;
+  bool order_rows = false;  // decode units launch longest row first (the order goes to the workspace)
   // workspace byte offsets
-  size_t d_count = 0, d_ml = 0, d_o = 0, t_count = 0, t_ml = 0, t_o = 0, total = 0;
+  size_t d_count = 0, d_ml = 0, d_o = 0, t_count = 0, t_ml = 0, t_o = 0, order = 0, total = 0;
 };
 
+// Whether a call's decode rows launch longest first (pa_set_unit_order).
+// Automatic: when the rows are many and a unit may be long (at least 1024
+// keys), so that a long unit started late could outlast the rest of the
+// launch by more than the order costs (one small launch, or one more CTA of
+// the step's append launch); a call of short rows keeps its order.
+bool want_order(int32_t mode, const pa_pool_desc& d, int32_t n_decode_rows, int32_t max_blocks, int32_t split_tokens) {
+  if (mode == PA_ORDER_CALL || n_decode_rows < 2) return false;
+  if (mode == PA_ORDER_LONGEST_FIRST) return true;
+  const long long longest_unit = std::min<long long>(static_cast<long long>(max_blocks) * d.page_size, split_tokens);
+  return n_decode_rows >= 128 && longest_unit >= 1024;
+}
+
 Plan make_plan(const pa_pool_desc& d, int32_t n_rows, int32_t hq, int32_t max_blocks, const pa_chunk* chunks,
-               int32_t n_chunks, bool tile_dtypes, int32_t split_tokens) {
+               int32_t n_chunks, bool tile_dtypes, int32_t split_tokens, int32_t order_mode) {
   Plan pl;
   pl.G = hq / d.num_kv_heads;
   pl.max_splits = max_splits_for(d, max_blocks, split_tokens);
@@ -126,6 +141,14 @@ Plan make_plan(const pa_pool_desc& d, int32_t n_rows, int32_t hq, int32_t max_bl
     off += pad(slots * 2 * sizeof(float));
     pl.t_o = off;
     off += pad(slots * d.head_dim * sizeof(float));
+  }
+  // the order's room is kept whenever the rows could want it (chunk rows that
+  // end up on the decode path count as decode rows), so that the workspace
+  // size for a bf16 pool covers either query dtype
+  if (want_order(order_mode, d, n_rows, max_blocks, split_tokens)) {
+    pl.order_rows = want_order(order_mode, d, n_rows - pl.total_rows, max_blocks, split_tokens);
+    pl.order = off;
+    off += pad(static_cast<size_t>(n_rows) * sizeof(int32_t));
   }
   pl.total = off;
   return pl;
@@ -312,7 +335,8 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
   if (!aligned(q, 16) || !aligned(out, 16)) return fail(PA_ERR_INVALID_ARG, "q / out must be 16-byte aligned");
   const int32_t split_tokens = g_split_tokens.load(std::memory_order_relaxed);  // one value for the plan and the kernels
   const Plan pl = make_plan(d, n_rows, num_q_heads, max_blocks_per_seq, chunks, n_chunks,
-                            q_dtype == PA_BF16 && d.kv_dtype == PA_BF16, split_tokens);
+                            q_dtype == PA_BF16 && d.kv_dtype == PA_BF16, split_tokens,
+                            g_unit_order.load(std::memory_order_relaxed));
   if (scratch != nullptr && pl.total > 0) {
     if (pl.total > scratch->bytes)
       return fail(PA_ERR_UNSUPPORTED,
@@ -414,6 +438,30 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
     p.vmap_dec = pool->vmap_dec;
   }
 
+  // Decode rows longest first: the order goes to the workspace, written by one
+  // CTA of its own launch, or of the step's append launch when there is one;
+  // the attention follows as its programmatic dependent.  Row groups keep the
+  // caller's order (a group is consecutive rows of the call).
+  const bool use_order = pl.order_rows && !(mma_e4m3 && p.row_group > 1);
+  pa::OrderParams ord{};
+  if (use_order) {
+    ord.seq_ids = seq_ids;
+    ord.positions = positions;
+    ord.n_rows = n_rows;
+    ord.num_seqs = num_seqs;
+    ord.max_pos = static_cast<int32_t>(std::min<long long>(static_cast<long long>(max_blocks_per_seq) * d.page_size,
+                                                           0x7fffffffLL));
+    ord.split_tokens = split_tokens;
+    ord.n_skip = p.n_chunks;
+    for (int c = 0; c < p.n_chunks; ++c) {
+      ord.skip_begin[c] = p.chunk_begin[c];
+      ord.skip_end[c] = p.chunk_end[c];
+    }
+    ord.order = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + pl.order);
+    p.row_order = ord.order;
+  }
+  bool order_in_append = false;
+
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (scratch != nullptr && pl.total > 0) {
     // the counters of the finished splits must start at zero; every partial
@@ -451,10 +499,20 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
         ap.range_begin[c] = chunks[c].row_begin;
         ap.range_first[c + 1] = ap.range_first[c] + chunks[c].n_rows;
       }
+      if (use_order) {
+        ap.with_order = 1;
+        ap.order = ord;
+        order_in_append = true;
+      }
       const cudaError_t ea = pa::launch_append(ap, s);
       if (ea != cudaSuccess) return cuda_fail(ea, "append launch");
       p.dependent = 1;
     }
+  }
+  if (use_order && !order_in_append) {
+    const cudaError_t eo = pa::launch_order_rows(ord, s);
+    if (eo != cudaSuccess) return cuda_fail(eo, "order launch");
+    p.dependent = 1;
   }
   cudaError_t e = cudaErrorNotSupported;
   if (p.n_prefill_ctas > 0) {
@@ -564,7 +622,8 @@ size_t pa_attention_workspace_bytes(const pa_pool* pool, int32_t n_rows, int32_t
     return 0;
   // chunks of a bf16 pool may take the tile path (with bf16 queries): size for it
   return make_plan(pool->desc, n_rows, num_q_heads, max_blocks_per_seq, chunks, n_chunks,
-                   pool->desc.kv_dtype == PA_BF16, g_split_tokens.load(std::memory_order_relaxed))
+                   pool->desc.kv_dtype == PA_BF16, g_split_tokens.load(std::memory_order_relaxed),
+                   g_unit_order.load(std::memory_order_relaxed))
       .total;
 }
 
@@ -610,6 +669,15 @@ pa_status pa_set_row_groups(int32_t rows) {
 }
 
 int32_t pa_get_row_groups(void) { return g_row_groups.load(std::memory_order_relaxed); }
+
+pa_status pa_set_unit_order(int32_t mode) {
+  if (mode != PA_ORDER_AUTO && mode != PA_ORDER_CALL && mode != PA_ORDER_LONGEST_FIRST)
+    return fail(PA_ERR_INVALID_ARG, "unit order %d is not PA_ORDER_AUTO, PA_ORDER_CALL or PA_ORDER_LONGEST_FIRST", mode);
+  g_unit_order.store(mode, std::memory_order_relaxed);
+  return PA_OK;
+}
+
+int32_t pa_get_unit_order(void) { return g_unit_order.load(std::memory_order_relaxed); }
 
 void pa_set_wait_limit(uint32_t microseconds) {
   g_wait_limit.store(microseconds == 0 ? pa::kDefaultWaitLimit : microseconds, std::memory_order_relaxed);

@@ -11,12 +11,16 @@
 //   f32 -> bf16                round to nearest even (cvt.rn.bf16.f32)
 //   f32|bf16 -> fp8 e4m3       IEEE binary32 division by the scale, then
 //                              satfinite round-to-nearest-even (cvt.rn.satfinite)
-#include "pa_device.cuh"
+#include "pa_order.cuh"
 
 namespace pa {
 
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendParams p) {
   griddep_launch_dependents();  // an attention launched as a dependent may start its lookups now
+  if (p.with_order && blockIdx.x == gridDim.x - 1) {  // the extra CTA: the decode rows' launch order
+    order_rows_block(p.order);
+    return;
+  }
   const long long oct_per_row = static_cast<long long>(p.Hkv) * p.D / 8;  // octets of one K (or V) row
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long rows = p.n_ranges > 0 ? p.range_first[p.n_ranges] : p.n_rows;
@@ -97,9 +101,9 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const long long rows = p.n_ranges > 0 ? p.range_first[p.n_ranges] : p.n_rows;
   const long long total = rows * 2 * p.Hkv * p.D / 8;
-  if (total <= 0) return cudaSuccess;
+  if (total <= 0 && !p.with_order) return cudaSuccess;
   const int threads = 256;
-  const long long blocks = (total + threads - 1) / threads;
+  const long long blocks = (total + threads - 1) / threads + (p.with_order ? 1 : 0);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
   count_launch();

@@ -358,6 +358,14 @@ __device__ __forceinline__ bool row_in_chunk(const AttnParams& p, int row) {
   return false;
 }
 
+// The row of decode-unit slot `slot`: the slot itself, or its entry in the
+// launch order that the preceding launch wrote (this launch depends on it)
+__device__ __forceinline__ int unit_row(const AttnParams& p, int slot) {
+  if (p.row_order == nullptr || slot >= p.n_rows) return slot;
+  griddep_wait();
+  return __ldcg(p.row_order + slot);
+}
+
 // Copy the valid token slots of stage n (tokens t_begin + 32n .. +32, clipped
 // to t_end) into ring slot s: one bulk copy of K and one of V per page piece.
 // P is a power of two (lg_p = log2 P).
@@ -624,7 +632,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int unit, unsig
   const int h = unit % p.Hkv;
   const int rest = unit / p.Hkv;
   const int split = rest % p.max_splits;
-  const int row = rest / p.max_splits;
+  const int row = unit_row(p, rest / p.max_splits);
   if (row >= p.n_rows) return;
   if (p.n_chunks > 0 && row_in_chunk(p, row)) return;
 

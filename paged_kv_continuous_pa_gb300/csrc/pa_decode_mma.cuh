@@ -443,7 +443,7 @@ __device__ __forceinline__ void decode_unit_mma(const AttnParams& p, int unit, u
   const int h = unit % p.Hkv;
   const int rest = unit / p.Hkv;
   const int split = rest % p.max_splits;
-  const int row = rest / p.max_splits;
+  const int row = unit_row(p, rest / p.max_splits);
   if (row >= p.n_rows) return;
   if (p.n_chunks > 0 && row_in_chunk(p, row)) return;
 

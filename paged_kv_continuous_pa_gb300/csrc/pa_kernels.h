@@ -50,6 +50,21 @@ constexpr int kMaxHeadScales = 64;  // kv heads a pool with per-head fp8 scales 
 // The scale entry of kv head h: per head, or the per-tensor entry 0.
 #define PA_HEAD(p, h) ((p).head_scales ? (h) : 0)
 
+// The launch order of a call's decode rows (pa_set_unit_order): a single
+// CTA writes the row indices longest first into `order`, either as a launch of
+// its own or as one more CTA of the append launch that precedes the attention.
+struct OrderParams {
+  const int32_t* seq_ids;
+  const int32_t* positions;
+  int32_t n_rows, num_seqs;
+  int32_t max_pos;        // max_blocks * P: positions at or past it are out of range
+  int32_t split_tokens;   // a unit holds at most this many keys
+  int32_t n_skip;         // rows of tile-path chunks: no decode units, listed last
+  int32_t skip_begin[kMaxChunks];
+  int32_t skip_end[kMaxChunks];
+  int32_t* order;         // out: [n_rows] row indices
+};
+
 struct AppendParams {
   void* k_pool;
   void* v_pool;
@@ -72,6 +87,10 @@ struct AppendParams {
   int32_t n_ranges;
   int32_t range_begin[kMaxChunks];
   int32_t range_first[kMaxChunks + 1];
+  // 1: one more CTA, after the rows' CTAs, writes `order` (the attention that
+  // follows as a programmatic dependent reads it)
+  int32_t with_order;
+  OrderParams order;
 };
 
 struct AttnParams {
@@ -112,6 +131,9 @@ struct AttnParams {
   float sm_scale_log2;                    // softmax scale * log2(e) for the tile path
   int32_t dependent;                      // host: launch as a programmatic dependent of the append
   int32_t row_group;                      // e4m3 tensor-core decode: rows per CTA (1, 2, 4 or 8)
+  // Decode units in launch order: unit slot i runs row row_order[i], written
+  // by the launch this one depends on (read after griddep_wait); null: row i
+  const int32_t* row_order;
   // pa_step: every row outside the caller's chunks appends its own new K/V
   // row inside the attention launch (the unit of its last split, per kv
   // head), with the encoder of the append kernel; chunk rows were appended
@@ -132,6 +154,10 @@ struct AttnParams {
 };
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+
+// One CTA that writes o.order (the rows longest first); the attention launched
+// after it as a programmatic dependent may start its setup at once.
+cudaError_t launch_order_rows(const OrderParams& o, cudaStream_t stream);
 
 // Let `kernel` use `bytes` of dynamic shared memory on the current device.
 // The attribute is per device, so it is set once for each device this process

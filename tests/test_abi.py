@@ -144,6 +144,32 @@ def test_row_groups_setting(lib):
         lib.pa_set_row_groups(old)
 
 
+def test_unit_order_setting(lib):
+    old = lib.pa_get_unit_order()
+    assert old == pa.PA_ORDER_AUTO
+    st, h = _create(lib, _desc())  # P 32, 2 kv heads, D 64
+    assert st == pa.PA_OK
+    try:
+        for bad in (-1, 3, 7):
+            assert lib.pa_set_unit_order(bad) == pa.PA_ERR_INVALID_ARG
+            assert lib.pa_get_unit_order() == old
+        ws = lambda n, mb, chunks=None: lib.pa_attention_workspace_bytes(h, n, 8, mb, chunks, 1 if chunks else 0)
+        # 40 pages of 32 tokens: units up to 1280 keys, never split; the order takes n_rows int32, padded to 256
+        assert lib.pa_set_unit_order(pa.PA_ORDER_AUTO) == pa.PA_OK
+        assert ws(200, 40) == 1024     # 200 rows: ordered
+        assert ws(127, 40) == 0        # too few rows to order
+        assert ws(200, 20) == 0        # units of at most 640 keys
+        whole = (pa.Chunk * 1)(pa.Chunk(0, 200))
+        assert ws(200, 40, whole) == 1024  # room kept although bf16 queries would run every row as a tile
+        assert lib.pa_set_unit_order(pa.PA_ORDER_CALL) == pa.PA_OK and lib.pa_get_unit_order() == pa.PA_ORDER_CALL
+        assert ws(200, 40) == 0
+        assert lib.pa_set_unit_order(pa.PA_ORDER_LONGEST_FIRST) == pa.PA_OK
+        assert ws(100, 20) == 512 and ws(1, 20) == 0
+    finally:
+        lib.pa_set_unit_order(old)
+        lib.pa_pool_destroy(h)
+
+
 def test_settings_change_from_other_threads(lib):
     """One thread flips the split length while others size workspaces: every
     answer is the one of the two settings, never a mix (a call reads it once)."""

@@ -127,3 +127,32 @@ def test_noalloc_rejects_calls_beyond_its_scratch():
     assert st == pa.PA_ERR_UNSUPPORTED
     assert "scratch" in pa.last_error()
 
+
+
+def test_noalloc_with_rows_longest_first():
+    """The decode rows' launch order (pa_set_unit_order) goes through the
+    shared array too: bytes equal to pa_attention's in both orders, twice."""
+    pa_build.build()
+    old = pa.get_unit_order()
+    wl = W.batched_decode(seed=31, n_seqs=48, ctx_lo=1, ctx_hi=1500)
+    st = pa_setup.upload(wl)
+    st.append_step()
+    torch.cuda.synchronize()
+    try:
+        outs = []
+        for mode in (pa.PA_ORDER_LONGEST_FIRST, pa.PA_ORDER_CALL, pa.PA_ORDER_LONGEST_FIRST):
+            pa.set_unit_order(mode)
+            ws = torch.zeros(max(pa.workspace_bytes(st.pool, wl.n_rows, wl.Hq, wl.max_blocks), 256), dtype=torch.uint8,
+                             device="cuda")
+            ref_out = torch.empty_like(st.q)
+            pa.attention(st.pool, st.q, st.seq_ids, st.positions, st.block_tables, ref_out, workspace=ws,
+                         status=st.status)
+            out = torch.full_like(st.q, float("nan"))
+            pa.attention_noalloc(st.pool, st.q, st.seq_ids, st.positions, st.block_tables, out, status=st.status)
+            torch.cuda.synchronize()
+            assert int(st.status.item()) == 0
+            assert _bits(out) == _bits(ref_out), f"order mode {mode}: output bytes differ from pa_attention"
+            outs.append(_bits(out))
+        assert outs[0] == outs[1] == outs[2]
+    finally:
+        pa.set_unit_order(old)
