@@ -49,12 +49,29 @@ __device__ __forceinline__ void order_rows_block(const OrderParams& o) {
     if (k >= 0 && (same & below) == 0) atomicAdd(&start[k], __popc(same));
   }
   __syncthreads();
-  if (tid == 0) {  // start[k] = rows with a larger key
-    int acc = 0;
-    for (int b = kOrderBins - 1; b >= 0; --b) {
-      const int c = start[b];
-      start[b] = acc;
-      acc += c;
+  if (tid < 32) {
+    // start[k] = rows with a larger key: an exclusive scan from the top key
+    // down, PER keys a lane, then across the lanes
+    constexpr int PER = (kOrderBins + 31) / 32;
+    int c[PER], sum = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int b = kOrderBins - 1 - (lane * PER + i);
+      c[i] = b >= 0 ? start[b] : 0;
+      sum += c[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int acc = incl - sum;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int b = kOrderBins - 1 - (lane * PER + i);
+      if (b >= 0) start[b] = acc;
+      acc += c[i];
     }
   }
   __syncthreads();
