@@ -258,10 +258,12 @@ int32_t pa_get_row_groups(void);
 /* Launch order of the decode rows.  A decode launch runs one CTA per (row,
  * split, kv head) and the GPU starts CTAs roughly in index order, so a long
  * row listed late starts in the last wave and runs on after the rest of the
- * launch has finished.  PA_ORDER_LONGEST_FIRST runs the units of the rows
- * with the most keys per unit first ("llm-rs ...", section "2. Why decode is
- * a memory problem": keep HBM busy to the end of the launch): one CTA, of a
- * launch of its own or of pa_step's append launch, sorts the rows by the key
+ * launch has finished, reading HBM at a fraction of its rate (the pages
+ * measure a kernel by its fraction of the bandwidth ceiling: "llm-rs ...",
+ * section "2. Why decode is a memory problem"; they describe no launch
+ * order).  PA_ORDER_LONGEST_FIRST runs the units of the rows with the most
+ * keys per unit first: one CTA, of a launch of its own or of pa_step's append
+ * launch, sorts the rows by the key
  * count of their longest unit into the workspace, and the attention launch
  * reads the order (its programmatic dependent).  PA_ORDER_CALL keeps the
  * call's order, one launch fewer.  PA_ORDER_AUTO (the default) orders a call
