@@ -3,12 +3,14 @@
 // A decode launch runs one CTA per (row, split, kv head), and the GPU starts
 // CTAs roughly in index order.  With the rows in the caller's order, a long
 // row whose units start in the last wave runs on after everything else has
-// finished, close to alone on the GPU; listing the rows by decreasing work
-// starts the long units in the first waves and lets the short ones fill the
-// end ("llm-rs ...", section "2. Why decode is a memory problem": the launch
-// should keep HBM busy to its end).  The order only decides where a row's
-// units run, never what they compute: a row's arithmetic and its output bits
-// are the same at any place in the order.
+// finished, close to alone on the GPU, and the launch's end reads HBM at a
+// fraction of its rate; listing the rows by decreasing work starts the long
+// units in the first waves and lets the short ones fill the end.  (The
+// yardstick is the fraction of the bandwidth ceiling a launch reaches,
+// "llm-rs ...", section "2. Why decode is a memory problem"; the pages
+// describe no launch order, this one is the library's own.)  The order only
+// decides where a row's units run, never what they compute: a row's
+// arithmetic and its output bits are the same at any place in the order.
 //
 // One CTA sorts the rows by counting: the key of a row is the number of
 // 32-token stages of its longest unit, min(position + 1, split length) / 32
