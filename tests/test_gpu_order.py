@@ -211,3 +211,29 @@ def test_timeout_reported_with_the_order_in_front():
     torch.cuda.synchronize()
     assert int(st.status.item()) == 0
     assert torch.equal(u8(st.out), good[1])
+
+
+def test_many_rows_in_several_passes():
+    """More rows than the order CTA has threads, in both places the order is
+    written: a launch of its own (1024 threads: 2500 rows) and the step's
+    append launch (256 threads: 700 decode rows beside a chunk)."""
+    rng = np.random.default_rng(5)
+    many = W._decode_workload("many", 91, rng.integers(1, 200, size=2500).tolist(), 2, 1, 64, 16, W.BF16, W.BF16,
+                              max_ctx=208, spare_pages=3, description="2500 short rows")
+    assert_same(run(many, pa.PA_ORDER_CALL, False), run(many, pa.PA_ORDER_LONGEST_FIRST, False), "2500 rows")
+    pa.set_unit_order(pa.PA_ORDER_LONGEST_FIRST)
+    st = pa_setup.upload(many)
+    st.append_step()
+    st.attend()
+    torch.cuda.synchronize()
+    order_bytes = (many.n_rows * 4 + 255) // 256 * 256
+    order = st.workspace.view(torch.int32)[(st.workspace.numel() - order_bytes) // 4:][: many.n_rows].cpu().numpy()
+    assert sorted(order.tolist()) == list(range(many.n_rows))
+    keys = np.array([_unit_key(int(many.positions[r]), pa.get_split_tokens()) for r in order])
+    assert (np.diff(keys) <= 0).all()
+    mixed = W.chunked_step(63, chunks=[(300, 40, 352)], decode_ctx=rng.integers(1, 400, size=700).tolist(), Hq=4,
+                           Hkv=2, D=64, P=16)
+    a = run(mixed, pa.PA_ORDER_CALL, True)
+    b = run(mixed, pa.PA_ORDER_LONGEST_FIRST, True)
+    assert a[2] == 0 and b[3] == a[3], "the append launch carries the order: no extra launch"
+    assert_same(a, b, "700 decode rows beside a chunk, pa_step")
