@@ -177,7 +177,9 @@ pa_status pa_attention(const pa_pool *pool, int32_t n_rows, const void *q, pa_dt
  *   - Rows outside every chunk (decode rows) append their own new K/V inside
  *     the attention launch: for each kv head, the attention unit that holds
  *     the row's position stores the row's converted key and value in the pool
- *     before it copies that page, so a step without chunks is ONE launch.
+ *     before it copies that page, so a step without chunks is ONE attention
+ *     launch (behind the one-CTA order launch when pa_set_unit_order orders
+ *     its rows; a step with chunks has its append launch write the order).
  *   - Chunk rows read one another's keys, so they are appended first by an
  *     append launch over the chunks' rows only; the attention kernel is its
  *     programmatic dependent (its CTAs start their lookups while the append
