@@ -374,6 +374,7 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
   p.q_is_bf16 = q_dtype == PA_BF16;
   p.split_tokens = split_tokens;
   p.max_splits = pl.max_splits;
+  p.n_unit_rows = n_rows;
   p.row_group = g_row_groups.load(std::memory_order_relaxed);
   // per kv head (or entry 0 for all): softmax scale * k scale * log2(e), and the v scale
   p.head_scales = pool->head_scales ? 1 : 0;
@@ -459,6 +460,7 @@ pa_status attention_impl(const pa_pool* pool, int32_t n_rows, const void* q, pa_
     }
     ord.order = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + pl.order);
     p.row_order = ord.order;
+    p.n_unit_rows = n_rows - pl.total_rows;  // the order lists every row but the tile-path chunks'
   }
   bool order_in_append = false;
 

@@ -361,7 +361,8 @@ __device__ __forceinline__ bool row_in_chunk(const AttnParams& p, int row) {
 // The row of decode-unit slot `slot`: the slot itself, or its entry in the
 // launch order that the preceding launch wrote (this launch depends on it)
 __device__ __forceinline__ int unit_row(const AttnParams& p, int slot) {
-  if (p.row_order == nullptr || slot >= p.n_rows) return slot;
+  if (p.row_order == nullptr) return slot;
+  if (slot >= p.n_unit_rows) return p.n_rows;  // no such unit: it exits
   griddep_wait();
   return __ldcg(p.row_order + slot);
 }
@@ -881,7 +882,7 @@ cudaError_t launch_decode_inst(const AttnParams& p0, cudaStream_t stream) {
   static std::atomic<unsigned long long> smem_done{0};  // devices on which the size is allowed
   const cudaError_t ea = allow_dynamic_smem(decode_kernel<D, G, KVT>, smem_done, smem);
   if (ea != cudaSuccess) return ea;
-  const long long units = static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
+  const long long units = static_cast<long long>(p.n_unit_rows) * p.max_splits * p.Hkv;
   if (units <= 0) return cudaSuccess;
   const cudaError_t e = launch_kernel(decode_kernel<D, G, KVT>, dim3(static_cast<unsigned>(units)), dim3(Geo::THREADS),
                                       smem, stream, p.dependent != 0, p);

@@ -944,7 +944,7 @@ cudaError_t launch_decode_mma_inst(const AttnParams& p, cudaStream_t stream) {
   if (p.row_group == 2) return launch_decode_mma_group<G, 2>(p, stream);
   if (p.row_group == 4) return launch_decode_mma_group<G, 4>(p, stream);
   if (p.row_group == 8) return launch_decode_mma_group<G, 8>(p, stream);
-  const long long units = static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
+  const long long units = static_cast<long long>(p.n_unit_rows) * p.max_splits * p.Hkv;
   if (units <= 0) return cudaSuccess;
   if (units > 0x7fffffffLL) return cudaErrorNotSupported;
   const unsigned u = static_cast<unsigned>(units);

@@ -409,7 +409,7 @@ long long mma_bf16_resident_units() {
 // Ring depth by the number of units, as for the e4m3 units (no effect on the bits).
 template <int G>
 cudaError_t launch_decode_mma_bf16_inst(const AttnParams& p, cudaStream_t stream) {
-  const long long units = static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
+  const long long units = static_cast<long long>(p.n_unit_rows) * p.max_splits * p.Hkv;
   if (units <= 0) return cudaSuccess;
   if (units > 0x7fffffffLL) return cudaErrorNotSupported;
   const unsigned u = static_cast<unsigned>(units);

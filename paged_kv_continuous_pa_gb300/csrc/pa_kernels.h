@@ -134,6 +134,9 @@ struct AttnParams {
   // Decode units in launch order: unit slot i runs row row_order[i], written
   // by the launch this one depends on (read after griddep_wait); null: row i
   const int32_t* row_order;
+  // rows that get decode units: n_rows, or with a launch order the rows it
+  // lists (every row but those of tile-path chunks)
+  int32_t n_unit_rows;
   // pa_step: every row outside the caller's chunks appends its own new K/V
   // row inside the attention launch (the unit of its last split, per kv
   // head), with the encoder of the append kernel; chunk rows were appended

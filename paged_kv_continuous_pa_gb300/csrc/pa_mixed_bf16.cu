@@ -47,7 +47,7 @@ cudaError_t launch_mixed_inst(const AttnParams& p0, cudaStream_t stream) {
   static std::atomic<unsigned long long> smem_done{0};  // devices on which the size is allowed
   const cudaError_t ea = allow_dynamic_smem(mixed_kernel<D, G>, smem_done, smem);
   if (ea != cudaSuccess) return ea;
-  const long long ctas = static_cast<long long>(p.n_prefill_ctas) + static_cast<long long>(p.n_rows) * p.max_splits * p.Hkv;
+  const long long ctas = static_cast<long long>(p.n_prefill_ctas) + static_cast<long long>(p.n_unit_rows) * p.max_splits * p.Hkv;
   if (ctas <= 0) return cudaSuccess;
   const cudaError_t e = launch_kernel(mixed_kernel<D, G>, dim3(static_cast<unsigned>(ctas)), dim3(Geo::THREADS), smem,
                                       stream, p.dependent != 0, p);

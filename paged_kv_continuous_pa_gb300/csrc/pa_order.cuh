@@ -14,8 +14,9 @@
 //
 // One CTA sorts the rows by counting: the key of a row is the number of
 // 32-token stages of its longest unit, min(position + 1, split length) / 32
-// rounded up; rows with no decode work (rows of tile-path chunks, rows whose
-// sequence or position is out of range) take key 0 and go last.  Rows with
+// rounded up; rows whose sequence or position is out of range take key 0 and
+// go last (their units write zeros and report the error), and rows of
+// tile-path chunks are left out (the launch has no decode units for them).  Rows with
 // equal keys keep no particular order.  Counting and placing go through
 // shared-memory atomics aggregated per warp over lanes of equal key, so a
 // batch of equal keys costs one atomic per warp.
@@ -29,7 +30,7 @@ constexpr int kOrderBins = kMaxSplitTokens / kStageTokens + 1;  // keys 0 .. spl
 
 __device__ __forceinline__ int order_key(const OrderParams& o, int r) {
   for (int c = 0; c < o.n_skip; ++c)
-    if (r >= o.skip_begin[c] && r < o.skip_end[c]) return 0;
+    if (r >= o.skip_begin[c] && r < o.skip_end[c]) return -1;  // left out: no decode units
   const int seq = __ldg(o.seq_ids + r), pos = __ldg(o.positions + r);
   if (seq < 0 || seq >= o.num_seqs || pos < 0 || pos >= o.max_pos) return 0;
   const int keys = min(pos + 1, o.split_tokens);
